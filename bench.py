@@ -1,0 +1,443 @@
+#!/usr/bin/env python3
+"""Benchmark of the BF16 attention leaf on GB300.
+
+One step = one call of the hot path (attn_dense_fwd, or attn_prefix_fwd for
+the prefix workload) over one batch of seeded synthetic bf16 inputs.  The
+metric is TFLOP/s with FLOPs = 4 * B * H * Nq * Nkv * D (2*D per score for
+Q K^T, 2*D for P V).  The default workload is dense B=1 N=4096 H=32 D=128.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload ID]
+    python bench.py --impl reference ...   # the FP64 CPU oracle, same metric
+
+Rank 0 prints one JSON line.  Under torchrun (N > 1) each rank runs an
+independent replica of the workload on its own GPU (no collective on the data
+path); the value is all ranks' FLOPs over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s and % of GB300 BF16 tensor peak (h32, d128/d64)"
+UNIT = "TFLOP/s"
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 512 << 20   # > 126 MB L2: written between timed iterations
+KERNEL_NAME = "ncp::attn_fwd_kernel"
+
+
+# ----------------------------------------------------------------------------
+# Helpers
+# ----------------------------------------------------------------------------
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"bf16_tflops": FALLBACK_BF16_TFLOPS, "hbm_gbs": 6800.0}, "fallback"
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "non_causal_prefix_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            doc = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = doc.get(workload_name)
+    if not ent or ent.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        import torch
+        self.gpu_id = None
+        try:
+            self.gpu_id = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+        except Exception:
+            self.gpu_id = None
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.gpu_id:
+            cmd.insert(1, f"--id={self.gpu_id}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+
+def make_call(ncp, w, dev_in, out):
+    if w.kind == "dense":
+        q, k, v = dev_in
+        return lambda stream=None: ncp.attn_dense_fwd(q, k, v, out, stream)
+    q, kp, vp, kc, vc = dev_in
+    return lambda stream=None: ncp.attn_prefix_fwd(q, kp, vp, kc, vc, out, stream)
+
+
+def time_device(torch, call, flush, steps, warmup, stream):
+    """Per-launch device time (ms) with CUDA events on the launching stream;
+    the L2 is flushed (a 512 MiB write) before every launch, outside the
+    events."""
+    for _ in range(warmup):
+        flush.add_(1)
+        call(stream)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            flush.add_(1)
+            starts[i].record(stream)
+            call(stream)
+            ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def time_e2e(torch, ncp, w, host_in, steps, warmup, stream):
+    """Host-to-host time per call: pinned host inputs copied in, the C-ABI
+    call, the output copied back, all inside the CUDA-event region."""
+    dev_in = [torch.empty_like(t, device="cuda") for t in host_in]
+    dev_out = torch.empty_like(dev_in[0])
+    host_out = torch.empty_like(host_in[0]).pin_memory()
+    call = make_call(ncp, w, dev_in, dev_out)
+
+    def one():
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        call(stream)
+        host_out.copy_(dev_out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(steps):
+            one()
+        end.record(stream)
+    torch.cuda.synchronize()
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    return start.elapsed_time(end) / steps, h2d, d2h
+
+
+def cpu_oracle_sample(w, inputs_cpu, target_s: float):
+    """The oracle, as it stands, on sampled output rows of workload ``w``:
+    FP64 TFLOP/s over the sample and the threads it used."""
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    oracle.set_threads(cores)
+    bits = [workloads.bf16_bits(t) for t in inputs_cpu]
+    fn = oracle.dense_attention_rows if w.kind == "dense" else oracle.prefix_attention_rows
+    total_rows = w.B * w.Nq * w.H
+    flops_per_row = 4 * w.n_keys * w.D
+    rng = np.random.default_rng(0)
+    n = min(total_rows, 256)
+    t0 = time.perf_counter()
+    fn(*bits, rng.integers(0, total_rows, n))
+    dt = time.perf_counter() - t0
+    n2 = int(min(total_rows, max(n, n * target_s / max(dt, 1e-6))))
+    rows = rng.integers(0, total_rows, n2)
+    t0 = time.perf_counter()
+    fn(*bits, rows)
+    dt = time.perf_counter() - t0
+    return {
+        "value": n2 * flops_per_row / dt / 1e12,
+        "unit": UNIT,
+        "cores": oracle.max_threads(),
+        "kind": "oracle",
+        "sample": f"{n2} of {total_rows} output rows (b,q,h) of {w.describe()}, "
+                  f"{dt:.1f} s of FP64 C/OpenMP",
+        "seconds": dt,
+    }
+
+
+def run_gpu(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    import non_causal_prefix_gb300 as ncp
+    if rank == 0 or world == 1:
+        ncp.build(quiet=True)
+    if world > 1:
+        torch.distributed.barrier()
+    ncp.load_library()
+
+    w = workloads.WORKLOADS[args.workload]
+    host_in = workloads.make_inputs(w)
+    dev_in = [t.cuda() for t in host_in]
+    out = torch.empty_like(dev_in[0])
+    call = make_call(ncp, w, dev_in, out)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    times = time_device(torch, call, flush, args.steps, args.warmup, stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clock_info = clocks.stop()
+    status, _ = ncp.device_status(stream)
+    if status != ncp.ATTN_OK:
+        raise RuntimeError(f"device status after timing: {ncp.status_string(status)}")
+
+    total_ms = sum(times)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * args.steps * w.flops / (total_ms / 1e3) / 1e12
+    ms_per_step = total_ms / args.steps
+
+    # End to end through the public API with host buffers.
+    host_pinned = [t.pin_memory() for t in host_in]
+    e2e_ms, h2d, d2h = time_e2e(torch, ncp, w, host_pinned, max(3, args.steps // 2), 2, stream)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * w.flops / (e2e_ms / 1e3) / 1e12
+
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
+    achieved = w.flops / (statistics.mean(times) / 1e3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0, sigma^2) rounded to bf16)",
+        "config": {
+            "workload": w.name,
+            "shape": w.describe(),
+            "flops_per_step": w.flops,
+            "l2": "512 MiB buffer written before every timed launch (inputs < L2)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "roofline": {
+            "bound": "tensor",
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "unit": UNIT,
+            "frac": round(achieved / peak, 4),
+            "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)",
+            "kernel": KERNEL_NAME + ("<128>" if w.D == 128 else "<64>"),
+            "traffic": recorded_traffic(w.name),
+        },
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": args.steps,
+        "clocks": clock_info,
+    }
+
+    if not args.no_configs and rank == 0 and world == 1:
+        line["per_config"] = per_config(torch, ncp, flush, stream, peak, args)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_oracle_sample(w, host_in, args.cpu_seconds)
+        line["cpu_baseline"].pop("seconds", None)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def per_config(torch, ncp, flush, stream, peak, args):
+    """Device TFLOP/s of every synthetic workload (context for the line)."""
+    res = {}
+    for cid, w in workloads.WORKLOADS.items():
+        dev_in = [t.cuda() for t in workloads.make_inputs(w)]
+        out = torch.empty_like(dev_in[0])
+        call = make_call(ncp, w, dev_in, out)
+        steps = max(3, min(args.steps, 20))
+        times = time_device(torch, call, flush, steps, 3, stream)
+        us = statistics.median(times) * 1e3
+        tf = w.flops / (us / 1e6) / 1e12
+        res[w.name] = {"median_us": round(us, 2), "tflops": round(tf, 1),
+                       "frac_of_peak": round(tf / peak, 4)}
+        del dev_in, out
+    torch.cuda.empty_cache()
+    return res
+
+
+# ----------------------------------------------------------------------------
+# Reference arm: the FP64 oracle on the host cores
+# ----------------------------------------------------------------------------
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = workloads.WORKLOADS[args.workload]
+    inputs = workloads.make_inputs(w)
+    per_step = max(1.0, 90.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, inputs, per_step / 4)
+    vals, secs = [], []
+    samples = []
+    for _ in range(args.steps):
+        r = cpu_oracle_sample(w, inputs, per_step)
+        vals.append(r["value"])
+        secs.append(r["seconds"])
+        samples.append(r)
+    value = statistics.median(vals)
+    last = samples[-1]
+    line = {
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * statistics.mean(secs), 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0, sigma^2) rounded to bf16)",
+        "impl": "reference",
+        "config": {"workload": w.name, "shape": w.describe(), "flops_per_step": w.flops},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": last["cores"],
+                         "kind": "oracle", "sample": last["sample"]},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__,
+                                 formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-config table")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,105 @@
+/*
+ * ncp_attn.h: C ABI of the GB300 (sm_103a) BF16 attention leaf.
+ *
+ * The operations are those of the page "Audit SGLang interfaces and refresh
+ * validated kernel solutions":
+ *   - attn_dense_fwd: definitions/dense_attention/noncausal_dense_attention_
+ *     h32_d128.json and noncausal_dense_attention_h32_d64.json, field
+ *     "reference": O = softmax(Q K^T * D^-0.5) V, no mask, FP32 accumulation,
+ *     BF16 output.
+ *   - attn_prefix_fwd: definitions/block_causal_attention/prefix_cached_block_
+ *     causal_h32_d128.json, field "reference": Q attends with full visibility
+ *     to keys cat(K_prefix, K_current) and values cat(V_prefix, V_current)
+ *     (prefix tokens first), scale D^-0.5.  No concatenated copy is made.
+ *
+ * Common conventions
+ *   Layout:     every tensor is a contiguous [B, N, H, D] bf16 array (token-
+ *               major, head, then head dim), the layout of the definitions'
+ *               "inputs" fields.
+ *   Memory:     all tensor pointers are DEVICE pointers owned by the caller on
+ *               the current CUDA device.  Inputs are read only; `out` is fully
+ *               overwritten and must not overlap any input.  The library
+ *               allocates no device memory per call.
+ *   Alignment:  every pointer must be 16-byte aligned (tensor-memory-access
+ *               descriptors require it).
+ *   Head dim:   D must be 64 or 128; H >= 1 (the definitions fix H = 32, any
+ *               H is accepted).  The scale is fixed to D^-0.5 (the definitions
+ *               expose no scale argument).
+ *   Streams:    work is enqueued on `stream` (0 = legacy default stream); the
+ *               calls return without synchronising.
+ *   Errors:     argument errors return a negative attn_status and launch
+ *               nothing.  A launch failure returns ATTN_ERR_CUDA.  Every wait
+ *               inside the kernels is bounded; a wait that gives up records a
+ *               device status that attn_device_status() returns as
+ *               ATTN_ERR_TIMEOUT.
+ */
+#ifndef NCP_ATTN_H
+#define NCP_ATTN_H
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_NULL = -1,     /* a required pointer is NULL */
+    ATTN_ERR_SHAPE = -2,    /* a size is out of range (B, N, Nq, Nc, H < 1; Np < 0; too large) */
+    ATTN_ERR_HEADDIM = -3,  /* D is not 64 or 128 */
+    ATTN_ERR_ALIGN = -4,    /* a pointer is not 16-byte aligned */
+    ATTN_ERR_ALIAS = -5,    /* out overlaps an input */
+    ATTN_ERR_CUDA = -6,     /* a CUDA runtime/driver call failed */
+    ATTN_ERR_TIMEOUT = -7   /* a bounded in-kernel wait gave up (see attn_device_status) */
+} attn_status;
+
+/*
+ * Dense non-causal self-attention.
+ *   q, k, v: [B, N, H, D] bf16, device, read only.
+ *   out:     [B, N, H, D] bf16, device, written.
+ * Returns ATTN_OK or a negative attn_status.
+ */
+int attn_dense_fwd(const void *q, const void *k, const void *v, void *out,
+                   int B, int N, int H, int D, cudaStream_t stream);
+
+/*
+ * Prefix-cached full-visibility attention.
+ *   q:      [B, Nq, H, D]
+ *   kp, vp: [B, Np, H, D]  cached prefix keys/values (may be NULL when Np == 0)
+ *   kc, vc: [B, Nc, H, D]  current keys/values
+ *   out:    [B, Nq, H, D]
+ * Each query attends to all Np + Nc keys, prefix first.  The definition
+ * requires Np >= 1 and Nc == Nq; this entry also accepts Np == 0 (dense
+ * attention over the current keys) and Nc != Nq (cross attention).
+ */
+int attn_prefix_fwd(const void *q, const void *kp, const void *vp, const void *kc,
+                    const void *vc, void *out, int B, int Nq, int Np, int Nc, int H, int D,
+                    cudaStream_t stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char *attn_status_string(int status);
+
+/*
+ * Synchronises `stream`, then returns ATTN_ERR_TIMEOUT if any kernel of this
+ * library recorded a bounded-wait failure since the previous call (and clears
+ * the record), ATTN_OK otherwise, or ATTN_ERR_CUDA if the synchronisation
+ * fails.  If `info` is not NULL it receives the first failure's site code
+ * (bits 0-7: wait site, bits 8-31: block index), or 0.
+ */
+int attn_device_status(cudaStream_t stream, unsigned int *info);
+
+/*
+ * Test hook.  mode 0: normal operation.  mode 1: in block 0 of the next
+ * launches, the loader skips the value tile of the second key/value tile, so
+ * the matrix-multiply role's wait for it runs out (needs at least two key
+ * tiles).  wait_limit_us sets the bound of every in-kernel wait (0 restores
+ * the default of 2 s).  Returns ATTN_OK, or ATTN_ERR_SHAPE for an unknown
+ * mode.  Host-side setting, applies to subsequent launches of this process.
+ */
+int attn_debug_set_fault(int mode, unsigned int wait_limit_us);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NCP_ATTN_H */

@@ -1,0 +1,163 @@
+"""ctypes binding of the C ABI declared in include/ncp_attn.h.
+
+Argument marshalling only: every step of the attention runs in the CUDA
+kernels of ``_lib/libncp_attn.so``.  There is no fallback; if the library is
+missing or cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+ATTN_OK = 0
+ATTN_ERR_NULL = -1
+ATTN_ERR_SHAPE = -2
+ATTN_ERR_HEADDIM = -3
+ATTN_ERR_ALIGN = -4
+ATTN_ERR_ALIAS = -5
+ATTN_ERR_CUDA = -6
+ATTN_ERR_TIMEOUT = -7
+
+# Every function the header declares, with its ctypes signature.
+_VP, _I, _UIP = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_uint)
+SIGNATURES = {
+    "attn_dense_fwd": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
+    "attn_prefix_fwd": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _VP]),
+    "attn_status_string": (ctypes.c_char_p, [_I]),
+    "attn_device_status": (_I, [_VP, _UIP]),
+    "attn_debug_set_fault": (_I, [_I, ctypes.c_uint]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    """A nonzero attn_status returned by the library."""
+
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library() -> ctypes.CDLL:
+    """Load the compiled library (it must exist: see ``build()``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"CUDA library {path} is missing: run non_causal_prefix_gb300.build()")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load_library().attn_status_string(int(status)).decode()
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, what: str):
+    if rc != ATTN_OK:
+        raise AttnError(rc, what)
+
+
+def _bnhd(t, name):
+    if t.dim() != 4:
+        raise ValueError(f"{name} must be [B, N, H, D]")
+    return t.shape
+
+
+def attn_dense_fwd(q, k, v, out, stream=None) -> None:
+    """Enqueue dense attention: q, k, v, out are CUDA bf16 [B, N, H, D] tensors."""
+    B, N, H, D = _bnhd(q, "q")
+    for t, n in ((k, "k"), (v, "v"), (out, "out")):
+        if tuple(t.shape) != (B, N, H, D):
+            raise ValueError(f"{n} must have q's shape {tuple(q.shape)}")
+    _check_tensors(q, k, v, out)
+    rc = load_library().attn_dense_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                       B, N, H, D, _stream_handle(stream))
+    _check(rc, "attn_dense_fwd")
+
+
+def attn_prefix_fwd(q, kp, vp, kc, vc, out, stream=None) -> None:
+    """Enqueue prefix-cached attention over cat(kp, kc) / cat(vp, vc).
+
+    kp/vp may be None or have Np == 0 (then only the current keys are used).
+    """
+    B, Nq, H, D = _bnhd(q, "q")
+    Bc, Nc, Hc, Dc = _bnhd(kc, "kc")
+    if (Bc, Hc, Dc) != (B, H, D) or tuple(vc.shape) != tuple(kc.shape):
+        raise ValueError("kc/vc must be [B, Nc, H, D] with q's B, H, D")
+    Np = 0 if kp is None else kp.shape[1]
+    if Np > 0 and (tuple(kp.shape) != (B, Np, H, D) or tuple(vp.shape) != tuple(kp.shape)):
+        raise ValueError("kp/vp must be [B, Np, H, D] with q's B, H, D")
+    if tuple(out.shape) != (B, Nq, H, D):
+        raise ValueError("out must have q's shape")
+    tensors = [q, kc, vc, out] + ([kp, vp] if Np > 0 else [])
+    _check_tensors(*tensors)
+    rc = load_library().attn_prefix_fwd(
+        q.data_ptr(), kp.data_ptr() if Np > 0 else None, vp.data_ptr() if Np > 0 else None,
+        kc.data_ptr(), vc.data_ptr(), out.data_ptr(), B, Nq, Np, Nc, H, D,
+        _stream_handle(stream))
+    _check(rc, "attn_prefix_fwd")
+
+
+def _check_tensors(*ts):
+    import torch
+    for t in ts:
+        if t.dtype != torch.bfloat16:
+            raise TypeError("tensors must be bfloat16")
+        if not t.is_cuda:
+            raise ValueError("tensors must be CUDA tensors")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous [B, N, H, D]")
+
+
+def dense_attention(q, k, v, stream=None):
+    """Allocate ``out`` with torch and run ``attn_dense_fwd``."""
+    import torch
+    out = torch.empty_like(q)
+    attn_dense_fwd(q, k, v, out, stream)
+    return out
+
+
+def prefix_attention(q, kp, vp, kc, vc, stream=None):
+    """Allocate ``out`` with torch and run ``attn_prefix_fwd``."""
+    import torch
+    out = torch.empty_like(q)
+    attn_prefix_fwd(q, kp, vp, kc, vc, out, stream)
+    return out
+
+
+def device_status(stream=None):
+    """(status, info) of attn_device_status: synchronises the stream."""
+    info = ctypes.c_uint(0)
+    rc = load_library().attn_device_status(_stream_handle(stream), ctypes.byref(info))
+    return rc, info.value
+
+
+def debug_set_fault(mode: int, wait_limit_us: int = 0) -> None:
+    _check(load_library().attn_debug_set_fault(int(mode), int(wait_limit_us)),
+           "attn_debug_set_fault")

@@ -1,0 +1,761 @@
+// Flash-style BF16 attention forward for GB300 (sm_103a): TMA-staged tiles,
+// tcgen05 MMAs accumulating S = Q K^T and O = P V in tensor memory (TMEM),
+// online softmax in registers, warp-specialised roles.
+//
+// Operations (page "Audit SGLang interfaces and refresh validated kernel
+// solutions"):
+//   dense:  definitions/dense_attention/noncausal_dense_attention_h32_d{128,64}
+//           .json, "reference" -- softmax(Q K^T * D^-0.5) V, no mask.
+//   prefix: definitions/block_causal_attention/prefix_cached_block_causal_h32_
+//           d128.json, "reference" -- keys/values are cat(prefix, current) on
+//           the token axis, every key visible.  The kernel walks the two
+//           segments through two pairs of TMA descriptors (no copy).
+//
+// CTA work unit: one (batch b, head h) and up to two 128-row query tiles.
+// Roles (320 threads):
+//   warps 0-3  softmax + correction + epilogue for query tile 0 (TMEM lanes 0-127)
+//   warps 4-7  the same for query tile 1
+//   warp 8     TMA producer (one elected lane)
+//   warp 9     TMEM allocator and tcgen05.mma issuer (one elected lane)
+// TMEM columns (512 allocated): S0 [0,128) S1 [128,256) O0 [256,256+D)
+// O1 [384,384+D).  P_i (bf16, two per 32-bit column) overwrites the first 64
+// columns of S_i once the softmax has read S_i into registers.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "ncp_attn.h"
+
+namespace ncp {
+
+constexpr int BM = 128;                  // query rows per tile (one TMEM lane each)
+constexpr int BN = 128;                  // keys per KV tile
+constexpr int NUM_THREADS = 320;
+constexpr int PRODUCER_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr uint32_t TMEM_COLS = 512;
+// TMEM column of S_i and O_i for query tile i.
+__host__ __device__ constexpr uint32_t tmem_s_col(int i) { return 128u * i; }
+__host__ __device__ constexpr uint32_t tmem_o_col(int i) { return 256u + 128u * i; }
+constexpr int MAX_SLOTS = 8;
+// Rescale O only when the running row maximum (log2 units) grows by more than
+// this; otherwise keep the stale maximum.  Exact, because the final 1/l uses
+// the same maximum as the accumulated O, and p <= 2^8 stays far from overflow.
+constexpr float RESCALE_THRESHOLD = 8.0f;
+
+template <int D>
+struct Cfg {
+  static constexpr int CHUNKS = D / 64;                  // 128-byte swizzle columns per row
+  static constexpr uint32_t TILE_BYTES = BN * D * 2;     // one K or V tile; one Q tile (BM == BN)
+  static constexpr uint32_t CHUNK_BYTES = BN * 128;      // 128 rows x 128 bytes
+  static constexpr int NSLOT = (D == 128) ? 4 : 8;       // K/V ring slots
+  static constexpr uint32_t RING_OFF = 0;
+  static constexpr uint32_t Q_OFF = RING_OFF + NSLOT * TILE_BYTES;
+  static constexpr uint32_t BAR_OFF = Q_OFF + 2 * TILE_BYTES;
+  static constexpr uint32_t SMEM_BYTES = BAR_OFF + 512 + 1024;  // barriers + 1 KiB alignment slack
+};
+
+struct SharedCtl {
+  uint64_t q_full;
+  uint64_t kv_full[MAX_SLOTS];
+  uint64_t kv_empty[MAX_SLOTS];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_full[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct Params {
+  CUtensorMap tm_q;
+  CUtensorMap tm_k[2];   // [0] prefix segment, [1] current segment
+  CUtensorMap tm_v[2];
+  __nv_bfloat16* out;
+  int Nq, H;
+  int n_tok[2];          // tokens per key segment
+  int n_tiles[2];        // KV tiles per key segment
+  float scale_log2;      // D^-0.5 * log2(e)
+  int fault_mode;
+  unsigned long long wait_limit_ns;
+};
+
+// Device-side status of bounded waits (module globals, not per call).
+__device__ unsigned int g_status;
+__device__ unsigned int g_status_info;
+
+// ----------------------------------------------------------------------------
+// PTX wrappers
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void record_timeout(int site) {
+  const unsigned int block =
+      blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  if (atomicCAS(&g_status, 0u, 1u) == 0u) g_status_info = (block << 8) | (site & 0xff);
+}
+
+// Slow path of wait_bounded: poll until the phase completes, the time limit
+// passes or another thread of the CTA has given up (abort flag).  A thread
+// that gives up first records the site.
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                       volatile int* abort_flag, int site) {
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      record_timeout(site);
+      return false;
+    }
+  }
+}
+
+// Wait for the phase of `bar` with parity `parity`, bounded in time.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                             volatile int* abort_flag, int site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, limit_ns, abort_flag, site);
+}
+
+// Bounded wait that ignores the abort flag: used to drain copies and MMAs in
+// flight before the CTA exits after an abort.
+__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > limit_ns) return;
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, int c3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor for tcgen05.mma, 128-byte swizzle.
+// Bits: [0,14) start>>4, [16,30) leading byte offset>>4, [32,46) stride byte
+// offset>>4, [46,48) version 1, [61,64) layout 2 = SWIZZLE_128B.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D f32 (bit 4), A bf16 (bits 7-9 = 1),
+// B bf16 (bits 10-12 = 1), A K-major, B K-major (0) or MN-major (bit 16),
+// N>>3 at bit 17, M>>4 at bit 24.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+#define NCP_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
+                  "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+#define NCP_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), \
+                  "r"(r[i + 4]), "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane -> registers.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : NCP_R8(0), NCP_R8(8), NCP_R8(16), NCP_R8(24)
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+          taddr),
+      NCP_W8(0), NCP_W8(8), NCP_W8(16), NCP_W8(24)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Warp-collective bounded wait: every lane waits, the warp proceeds only if
+// all lanes saw the phase complete.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t limit,
+                                          volatile int* abort_flag, int site) {
+  bool ok = wait_bounded(bar, parity, limit, abort_flag, site);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// ----------------------------------------------------------------------------
+// The kernel
+// ----------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ Params p) {
+  using C = Cfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment for the 128-byte swizzle atoms.
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (base_u32 - raw_u32);
+  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(base + C::BAR_OFF);
+  volatile int* abort_flag = &ctl->abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+  const int q0 = blockIdx.x * (2 * BM);
+  const bool two_tiles = (q0 + BM) < p.Nq;
+  const int T0 = p.n_tiles[0];
+  const int T = T0 + p.n_tiles[1];
+  const uint64_t limit = p.wait_limit_ns;
+
+  const uint32_t ring = base_u32 + C::RING_OFF;
+  const uint32_t qs = base_u32 + C::Q_OFF;
+  const uint32_t bar_q = smem_u32(&ctl->q_full);
+  auto bar_kv_full = [&](int s) { return smem_u32(&ctl->kv_full[s]); };
+  auto bar_kv_empty = [&](int s) { return smem_u32(&ctl->kv_empty[s]); };
+  const uint32_t bar_s[2] = {smem_u32(&ctl->s_full[0]), smem_u32(&ctl->s_full[1])};
+  const uint32_t bar_p[2] = {smem_u32(&ctl->p_full[0]), smem_u32(&ctl->p_full[1])};
+  const uint32_t bar_o[2] = {smem_u32(&ctl->o_full[0]), smem_u32(&ctl->o_full[1])};
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q, 1);
+    for (int s = 0; s < C::NSLOT; ++s) {
+      mbar_init(bar_kv_full(s), 1);
+      mbar_init(bar_kv_empty(s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_s[i], 1);
+      mbar_init(bar_p[i], 4);  // one arrival per softmax warp
+      mbar_init(bar_o[i], 1);
+    }
+    mbar_init(smem_u32(&ctl->drain), 1);
+    ctl->abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == MMA_WARP) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&ctl->tmem_base)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == PRODUCER_WARP) {
+    // ---------------------------------------------------------------- loader
+    if (lane == 0) {
+      prefetch_tmap(&p.tm_q);
+      for (int s = 0; s < 2; ++s) {
+        prefetch_tmap(&p.tm_k[s]);
+        prefetch_tmap(&p.tm_v[s]);
+      }
+      const int nq_tiles = two_tiles ? 2 : 1;
+      mbar_expect_tx(bar_q, nq_tiles * C::TILE_BYTES);
+      for (int i = 0; i < nq_tiles; ++i)
+        for (int c = 0; c < C::CHUNKS; ++c)
+          tma_load_4d(qs + i * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tm_q, c * 64, h,
+                      q0 + i * BM, b, bar_q);
+      int slot = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_parity = 0;  // per slot: a load was issued / its phase
+      bool ok = true;
+      for (int t = 0; t < T && ok; ++t) {
+        const int seg = (t < T0) ? 0 : 1;
+        const int tok0 = (t - (seg ? T0 : 0)) * BN;
+        for (int kind = 0; kind < 2; ++kind) {
+          ok = wait_bounded(bar_kv_empty(slot), phase ^ 1u, limit, abort_flag, 1);
+          if (!ok) break;
+          const bool skip = (p.fault_mode == 1) && kind == 1 && t == 1 && blockIdx.x == 0 &&
+                            blockIdx.y == 0 && blockIdx.z == 0;
+          if (!skip) {
+            const CUtensorMap* map = kind == 0 ? &p.tm_k[seg] : &p.tm_v[seg];
+            mbar_expect_tx(bar_kv_full(slot), C::TILE_BYTES);
+            for (int c = 0; c < C::CHUNKS; ++c)
+              tma_load_4d(ring + slot * C::TILE_BYTES + c * C::CHUNK_BYTES, map, c * 64, h, tok0,
+                          b, bar_kv_full(slot));
+            issued |= 1u << slot;
+            issued_parity = (issued_parity & ~(1u << slot)) | (phase << slot);
+          }
+          if (++slot == C::NSLOT) {
+            slot = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Abort: let every copy in flight land before the CTA exits.
+        wait_drain(bar_q, 0, limit);
+        for (int s = 0; s < C::NSLOT; ++s)
+          if (issued & (1u << s)) wait_drain(bar_kv_full(s), (issued_parity >> s) & 1u, limit);
+      }
+    }
+    __syncwarp();
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = make_idesc(BM, BN, false);
+      constexpr uint32_t IDESC_PV = make_idesc(BM, D, true);
+      const int nq = two_tiles ? 2 : 1;
+      // S_i = Q_i K^T over D in K-steps of 16 (32 bytes inside a 128-byte row).
+      auto issue_s = [&](int i, int k_slot) {
+        const uint32_t qa = qs + i * C::TILE_BYTES;
+        const uint32_t kb = ring + k_slot * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+          mma_ss(tmem + tmem_s_col(i), sw128_desc(qa + off, 16, 1024),
+                 sw128_desc(kb + off, 16, 1024), IDESC_S, kk > 0);
+        }
+      };
+      // O_i += P_i V over the BN keys in K-steps of 16 rows of V (MN-major B).
+      auto issue_pv = [&](int i, int v_slot, bool accumulate) {
+        const uint32_t vb = ring + v_slot * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(tmem + tmem_o_col(i), tmem + tmem_s_col(i) + kk * 8,
+                 sw128_desc(vb + kk * 16 * 128, C::CHUNK_BYTES, 1024), IDESC_PV,
+                 (accumulate || kk > 0) ? 1u : 0u);
+      };
+
+      bool ok = wait_bounded(bar_q, 0, limit, abort_flag, 2);
+      int slot = 0;
+      uint32_t phase = 0;
+      int v_prev = -1;
+      for (int j = 0; j < T && ok; ++j) {
+        const int k_slot = slot;
+        ok = wait_bounded(bar_kv_full(k_slot), phase, limit, abort_flag, 3);
+        if (!ok) break;
+        if (++slot == C::NSLOT) { slot = 0; phase ^= 1u; }
+        tc_fence_after();
+        for (int i = 0; i < nq && ok; ++i) {
+          if (j > 0) {
+            ok = wait_bounded(bar_p[i], (j - 1) & 1, limit, abort_flag, 4);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(i, v_prev, j - 1 > 0);
+          }
+          issue_s(i, k_slot);
+          mma_commit(bar_s[i]);
+        }
+        if (!ok) break;
+        if (j > 0) mma_commit(bar_kv_empty(v_prev));
+        mma_commit(bar_kv_empty(k_slot));
+        const int v_slot = slot;
+        ok = wait_bounded(bar_kv_full(v_slot), phase, limit, abort_flag, 5);
+        if (!ok) break;
+        if (++slot == C::NSLOT) { slot = 0; phase ^= 1u; }
+        v_prev = v_slot;
+      }
+      for (int i = 0; i < nq && ok; ++i) {
+        ok = wait_bounded(bar_p[i], (T - 1) & 1, limit, abort_flag, 6);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(i, v_prev, T - 1 > 0);
+        mma_commit(bar_o[i]);
+      }
+      if (ok) mma_commit(bar_kv_empty(v_prev));
+      if (!ok) {
+        // Abort: let every MMA in flight finish before TMEM is released.
+        mma_commit(smem_u32(&ctl->drain));
+        wait_drain(smem_u32(&ctl->drain), 0, limit);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------- softmax / correction / store
+    const int i = warp >> 2;  // query tile
+    const int wq = warp & 3;  // TMEM lane quarter
+    if (i == 0 || two_tiles) {
+      const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+      const uint32_t s_addr = tmem + lane_base + tmem_s_col(i);
+      const uint32_t o_addr = tmem + lane_base + tmem_o_col(i);
+      const float sl2 = p.scale_log2;
+      float m = -INFINITY;  // running (possibly stale) maximum, log2 units
+      float l = 0.f;        // running sum of exp2(x - m)
+      bool ok = true;
+      for (int j = 0; j < T; ++j) {
+        ok = warp_wait(bar_s[i], j & 1, limit, abort_flag, 7);
+        if (!ok) break;
+        tc_fence_after();
+        float s[BN];
+        {
+          uint32_t r[BN];
+#pragma unroll
+          for (int c = 0; c < BN; c += 32) tmem_ld32(s_addr + c, r + c);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(r[c]);
+        }
+        // Keys past the end of this segment: TMA filled them with zeros, their
+        // scores must be -inf instead.
+        const int seg = (j < T0) ? 0 : 1;
+        const int valid = p.n_tok[seg] - (j - (seg ? T0 : 0)) * BN;
+        if (valid < BN) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            if (c >= valid) s[c] = -INFINITY;
+        }
+        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+        for (int c = 4; c < BN; c += 4) {
+          mx0 = fmaxf(mx0, s[c]);
+          mx1 = fmaxf(mx1, s[c + 1]);
+          mx2 = fmaxf(mx2, s[c + 2]);
+          mx3 = fmaxf(mx3, s[c + 3]);
+        }
+        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        float alpha = 1.f;
+        bool rescale = false;
+        if (m_tile > m + RESCALE_THRESHOLD) {
+          alpha = ex2(m - m_tile);
+          l *= alpha;
+          m = m_tile;
+          rescale = (j > 0);
+        }
+        const float neg_m = -m;
+        float rs0 = 0.f, rs1 = 0.f;
+        uint32_t pk[BN / 2];
+#pragma unroll
+        for (int c = 0; c < BN / 2; ++c) {
+          const float p0 = ex2(fmaf(s[2 * c], sl2, neg_m));
+          const float p1 = ex2(fmaf(s[2 * c + 1], sl2, neg_m));
+          rs0 += p0;
+          rs1 += p1;
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        l += rs0 + rs1;
+        tmem_st32(s_addr + 0, pk);
+        tmem_st32(s_addr + 32, pk + 32);
+        if (__any_sync(0xffffffffu, rescale)) {
+          // O_i holds the complete sum through tile j-1: S_i(j) was issued
+          // after P_i(j-1) V and its commit has fired.  Rows of this warp that
+          // keep their maximum scale by 1.
+#pragma unroll
+          for (int c = 0; c < D; c += 32) {
+            uint32_t r[32];
+            tmem_ld32(o_addr + c, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st32(o_addr + c, r);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_p[i]);
+      }
+      if (ok) ok = warp_wait(bar_o[i], 0, limit, abort_flag, 8);
+      if (ok) {
+        tc_fence_after();
+        const int q = q0 + i * BM + wq * 32 + lane;
+        const float inv_l = 1.f / l;
+        __nv_bfloat16* orow = p.out + ((static_cast<size_t>(b) * p.Nq + q) * p.H + h) * D;
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(o_addr + c, r);
+          tmem_wait_ld();
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l,
+                               __uint_as_float(r[2 * e + 1]) * inv_l);
+          if (q < p.Nq) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+}  // namespace ncp
+
+// ============================================================================
+// Host side: argument checks, TMA descriptors, launch
+// ============================================================================
+namespace {
+
+using ncp::Params;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(ptr);
+  }();
+  return fn;
+}
+
+std::mutex g_cfg_mutex;
+int g_fault_mode = 0;
+unsigned long long g_wait_limit_ns = 2000000000ull;
+
+// [B, N, H, D] bf16, box of 64 head-dim elements x 1 head x 128 tokens x 1
+// batch, 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap* map, const void* base, int B, int N, int H, int D) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(H) * D * 2,
+                                 static_cast<cuuint64_t>(N) * H * D * 2};
+  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+template <int D>
+int launch(Params& prm, int B, int Nq, int H, cudaStream_t stream) {
+  using C = ncp::Cfg<D>;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  static bool configured[64] = {};
+  if (dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
+  if (!configured[dev]) {
+    if (cudaFuncSetAttribute(ncp::attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    configured[dev] = true;
+  }
+  const dim3 grid((Nq + 2 * ncp::BM - 1) / (2 * ncp::BM), H, B);
+  ncp::attn_fwd_kernel<D><<<grid, ncp::NUM_THREADS, C::SMEM_BYTES, stream>>>(prm);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int run(const void* q, const void* kp, const void* vp, const void* kc, const void* vc, void* out,
+        int B, int Nq, int Np, int Nc, int H, int D, cudaStream_t stream) {
+  if (!q || !kc || !vc || !out || (Np > 0 && (!kp || !vp))) return ATTN_ERR_NULL;
+  if (B < 1 || Nq < 1 || Nc < 1 || H < 1 || Np < 0) return ATTN_ERR_SHAPE;
+  if (H > 65535 || B > 65535) return ATTN_ERR_SHAPE;
+  if (D != 64 && D != 128) return ATTN_ERR_HEADDIM;
+  if (misaligned(q) || misaligned(kc) || misaligned(vc) || misaligned(out) ||
+      (Np > 0 && (misaligned(kp) || misaligned(vp))))
+    return ATTN_ERR_ALIGN;
+  const size_t row = static_cast<size_t>(H) * D * 2;
+  const size_t q_bytes = static_cast<size_t>(B) * Nq * row;
+  const size_t c_bytes = static_cast<size_t>(B) * Nc * row;
+  const size_t p_bytes = static_cast<size_t>(B) * Np * row;
+  if (overlaps(out, q_bytes, q, q_bytes) || overlaps(out, q_bytes, kc, c_bytes) ||
+      overlaps(out, q_bytes, vc, c_bytes) ||
+      (Np > 0 && (overlaps(out, q_bytes, kp, p_bytes) || overlaps(out, q_bytes, vp, p_bytes))))
+    return ATTN_ERR_ALIAS;
+
+  Params prm;
+  if (!make_map(&prm.tm_q, q, B, Nq, H, D)) return ATTN_ERR_CUDA;
+  if (!make_map(&prm.tm_k[1], kc, B, Nc, H, D) || !make_map(&prm.tm_v[1], vc, B, Nc, H, D))
+    return ATTN_ERR_CUDA;
+  if (Np > 0) {
+    if (!make_map(&prm.tm_k[0], kp, B, Np, H, D) || !make_map(&prm.tm_v[0], vp, B, Np, H, D))
+      return ATTN_ERR_CUDA;
+  } else {
+    prm.tm_k[0] = prm.tm_k[1];
+    prm.tm_v[0] = prm.tm_v[1];
+  }
+  prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.Nq = Nq;
+  prm.H = H;
+  prm.n_tok[0] = Np;
+  prm.n_tok[1] = Nc;
+  prm.n_tiles[0] = (Np + ncp::BN - 1) / ncp::BN;
+  prm.n_tiles[1] = (Nc + ncp::BN - 1) / ncp::BN;
+  prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+  {
+    std::lock_guard<std::mutex> lock(g_cfg_mutex);
+    prm.fault_mode = g_fault_mode;
+    prm.wait_limit_ns = g_wait_limit_ns;
+  }
+  return D == 128 ? launch<128>(prm, B, Nq, H, stream) : launch<64>(prm, B, Nq, H, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_dense_fwd(const void* q, const void* k, const void* v, void* out, int B, int N, int H,
+                   int D, cudaStream_t stream) {
+  if (!k || !v) return ATTN_ERR_NULL;
+  return run(q, nullptr, nullptr, k, v, out, B, N, 0, N, H, D, stream);
+}
+
+int attn_prefix_fwd(const void* q, const void* kp, const void* vp, const void* kc, const void* vc,
+                    void* out, int B, int Nq, int Np, int Nc, int H, int D, cudaStream_t stream) {
+  return run(q, kp, vp, kc, vc, out, B, Nq, Np, Nc, H, D, stream);
+}
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_NULL: return "null pointer";
+    case ATTN_ERR_SHAPE: return "size out of range";
+    case ATTN_ERR_HEADDIM: return "head dim must be 64 or 128";
+    case ATTN_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case ATTN_ERR_ALIAS: return "output overlaps an input";
+    case ATTN_ERR_CUDA: return "CUDA call failed";
+    case ATTN_ERR_TIMEOUT: return "in-kernel wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int attn_device_status(cudaStream_t stream, unsigned int* info) {
+  if (info) *info = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  unsigned int st = 0, inf = 0;
+  if (cudaMemcpyFromSymbol(&st, ncp::g_status, sizeof st) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (st == 0) return ATTN_OK;
+  if (cudaMemcpyFromSymbol(&inf, ncp::g_status_info, sizeof inf) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  const unsigned int zero = 0;
+  if (cudaMemcpyToSymbol(ncp::g_status, &zero, sizeof zero) != cudaSuccess ||
+      cudaMemcpyToSymbol(ncp::g_status_info, &zero, sizeof zero) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (info) *info = inf;
+  return ATTN_ERR_TIMEOUT;
+}
+
+int attn_debug_set_fault(int mode, unsigned int wait_limit_us) {
+  if (mode < 0 || mode > 1) return ATTN_ERR_SHAPE;
+  std::lock_guard<std::mutex> lock(g_cfg_mutex);
+  g_fault_mode = mode;
+  g_wait_limit_ns = wait_limit_us ? static_cast<unsigned long long>(wait_limit_us) * 1000ull
+                                  : 2000000000ull;
+  return ATTN_OK;
+}
+
+}  // extern "C"
