@@ -68,8 +68,10 @@ def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "non_causal_prefix_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+        path = os.path.join(csrc, f)
+        if os.path.isfile(path) and f.endswith((".cu", ".cuh", ".h")):
+            with open(path, "rb") as fh:
+                h.update(fh.read())
     return h.hexdigest()[:16]
 
 

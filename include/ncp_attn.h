@@ -98,6 +98,16 @@ int attn_device_status(cudaStream_t stream, unsigned int *info);
  */
 int attn_debug_set_fault(int mode, unsigned int wait_limit_us);
 
+/*
+ * Test hook: y[i] = 2^x[i] for i < n through one of the two exponential paths
+ * of the softmax: mode 0 the FMA-pipe polynomial (Cody-Waite reduction and a
+ * minimax cubic, relative error <= 1.02e-4 for -126 <= x <= 127, exactly 0 for
+ * x <= -127), mode 1 the hardware ex2.approx unit.  x and y are device
+ * pointers to n floats (caller-owned); enqueued on `stream`.  Returns ATTN_OK,
+ * ATTN_ERR_NULL, ATTN_ERR_SHAPE (n < 0, bad mode) or ATTN_ERR_CUDA.
+ */
+int attn_debug_exp2(const float *x, float *y, long long n, int mode, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

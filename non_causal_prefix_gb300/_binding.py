@@ -29,6 +29,7 @@ SIGNATURES = {
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_device_status": (_I, [_VP, _UIP]),
     "attn_debug_set_fault": (_I, [_I, ctypes.c_uint]),
+    "attn_debug_exp2": (_I, [_VP, _VP, ctypes.c_longlong, _I, _VP]),
 }
 
 _lock = threading.Lock()
@@ -156,6 +157,18 @@ def device_status(stream=None):
     info = ctypes.c_uint(0)
     rc = load_library().attn_device_status(_stream_handle(stream), ctypes.byref(info))
     return rc, info.value
+
+
+def debug_exp2(x, mode: int, stream=None):
+    """2^x on the GPU through the softmax's polynomial (mode 0) or MUFU (mode 1)
+    exponential; x is a CUDA float32 tensor, returns a new tensor."""
+    import torch
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA float32 tensor")
+    y = torch.empty_like(x)
+    _check(load_library().attn_debug_exp2(x.data_ptr(), y.data_ptr(), x.numel(), int(mode),
+                                          _stream_handle(stream)), "attn_debug_exp2")
+    return y
 
 
 def debug_set_fault(mode: int, wait_limit_us: int = 0) -> None:

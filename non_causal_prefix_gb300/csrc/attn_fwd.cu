@@ -57,6 +57,13 @@ struct Cfg {
   static constexpr uint32_t Q_OFF = RING_OFF + NSLOT * TILE_BYTES;
   static constexpr uint32_t BAR_OFF = Q_OFF + 2 * TILE_BYTES;
   static constexpr uint32_t SMEM_BYTES = BAR_OFF + 512 + 1024;  // barriers + 1 KiB alignment slack
+  // Share of the exponentials computed by the FMA-pipe polynomial instead of
+  // the MUFU unit: POLY_NUM of every POLY_DEN packed pairs.  The MUFU unit does
+  // 16 exp2 per clock per SM, as many as the S and P V MMAs need at D = 128;
+  // at D = 64 the MMAs need half the time, so more moves to the polynomial.
+  static constexpr int POLY_NUM = (D == 128) ? 1 : 1;
+  static constexpr int POLY_DEN = (D == 128) ? 4 : 2;
+  __host__ __device__ static constexpr bool poly_pair(int c) { return (c % POLY_DEN) >= POLY_DEN - POLY_NUM; }
 };
 
 struct SharedCtl {
@@ -75,7 +82,7 @@ struct Params {
   CUtensorMap tm_q;
   CUtensorMap tm_k[2];   // [0] prefix segment, [1] current segment
   CUtensorMap tm_v[2];
-  __nv_bfloat16* out;
+  CUtensorMap tm_o;      // output, same box and swizzle as Q
   int Nq, H;
   int n_tok[2];          // tokens per key segment
   int n_tiles[2];        // KV tiles per key segment
@@ -176,6 +183,87 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                             int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_commit_and_drain() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void named_barrier(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Two fp32 values in one 64-bit register pair, for the packed f32x2 ALU ops.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void up2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fsub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.ftz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// 2^x for a pair of exponents on the FMA/ALU pipes instead of the MUFU unit.
+// Cody-Waite style reduction x = j + f, j = round(x) (added to the exponent
+// field), f in [-1/2, 1/2]; 2^f by the minimax cubic p(f) = 1 + f (C1 + f (C2
+// + f C3)), relative error <= 1.02e-4 (coefficients from exp2_poly_coeffs.py).
+// x is clamped to >= -127: x = -127 (and -inf) give exactly +0, since p(0) = 1.
+// Valid for x <= 127.
+constexpr float EXP2_C1 = 0x1.62f5fap-1f;
+constexpr float EXP2_C2 = 0x1.f00c4ep-3f;
+constexpr float EXP2_C3 = 0x1.c2a25cp-5f;
+constexpr float ROUND_MAGIC = 12582912.0f;  // 1.5 * 2^23: x + M keeps round(x) in the low bits
+
+__device__ __forceinline__ void exp2_poly2(uint64_t x2, float& y0, float& y1) {
+  float a, b;
+  up2(x2, a, b);
+  const uint64_t x = pk2(fmaxf(a, -127.f), fmaxf(b, -127.f));
+  const uint64_t t = fadd2(x, pk2(ROUND_MAGIC, ROUND_MAGIC));
+  const uint64_t f = fsub2(x, fadd2(t, pk2(-ROUND_MAGIC, -ROUND_MAGIC)));
+  uint64_t p = ffma2(pk2(EXP2_C3, EXP2_C3), f, pk2(EXP2_C2, EXP2_C2));
+  p = ffma2(p, f, pk2(EXP2_C1, EXP2_C1));
+  p = ffma2(p, f, pk2(1.f, 1.f));
+  float p0, p1, t0, t1;
+  up2(p, p0, p1);
+  up2(t, t0, t1);
+  y0 = __uint_as_float(__float_as_uint(p0) + (__float_as_uint(t0) << 23));
+  y1 = __uint_as_float(__float_as_uint(p1) + (__float_as_uint(t1) << 23));
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -347,6 +435,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ---------------------------------------------------------------- loader
     if (lane == 0) {
       prefetch_tmap(&p.tm_q);
+      prefetch_tmap(&p.tm_o);
       for (int s = 0; s < 2; ++s) {
         prefetch_tmap(&p.tm_k[s]);
         prefetch_tmap(&p.tm_v[s]);
@@ -472,6 +561,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t s_addr = tmem + lane_base + tmem_s_col(i);
       const uint32_t o_addr = tmem + lane_base + tmem_o_col(i);
       const float sl2 = p.scale_log2;
+      const uint64_t sl2x2 = pk2(sl2, sl2);
       float m = -INFINITY;  // running (possibly stale) maximum, log2 units
       float l = 0.f;        // running sum of exp2(x - m)
       bool ok = true;
@@ -497,15 +587,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int c = 0; c < BN; ++c)
             if (c >= valid) s[c] = -INFINITY;
         }
-        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+        // Row maximum: four independent chains of 3-input max.
+        float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
+        float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
 #pragma unroll
-        for (int c = 4; c < BN; c += 4) {
-          mx0 = fmaxf(mx0, s[c]);
-          mx1 = fmaxf(mx1, s[c + 1]);
-          mx2 = fmaxf(mx2, s[c + 2]);
-          mx3 = fmaxf(mx3, s[c + 3]);
+        for (int c = 12; c + 8 <= BN; c += 8) {
+          mx0 = fmax3(mx0, s[c], s[c + 1]);
+          mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+          mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+          mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
         }
-        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        mx0 = fmax3(mx0, s[BN - 4], s[BN - 3]);
+        mx1 = fmax3(mx1, s[BN - 2], s[BN - 1]);
+        const float m_tile = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
         float alpha = 1.f;
         bool rescale = false;
         if (m_tile > m + RESCALE_THRESHOLD) {
@@ -514,32 +608,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           m = m_tile;
           rescale = (j > 0);
         }
-        const float neg_m = -m;
-        float rs0 = 0.f, rs1 = 0.f;
+        // p = 2^(s * scale * log2(e) - m) on packed pairs; pairs selected by
+        // PolySel go through the FMA-pipe polynomial, the rest through MUFU.
+        const uint64_t neg_m2 = pk2(-m, -m);
+        uint64_t acc0 = 0, acc1 = 0;  // two packed running sums (bits 0 = 0.0f)
         uint32_t pk[BN / 2];
 #pragma unroll
         for (int c = 0; c < BN / 2; ++c) {
-          const float p0 = ex2(fmaf(s[2 * c], sl2, neg_m));
-          const float p1 = ex2(fmaf(s[2 * c + 1], sl2, neg_m));
-          rs0 += p0;
-          rs1 += p1;
+          const uint64_t x = ffma2(pk2(s[2 * c], s[2 * c + 1]), sl2x2, neg_m2);
+          float p0, p1;
+          if (Cfg<D>::poly_pair(c)) {
+            exp2_poly2(x, p0, p1);
+          } else {
+            float x0, x1;
+            up2(x, x0, x1);
+            p0 = ex2(x0);
+            p1 = ex2(x1);
+          }
+          if (c & 1)
+            acc1 = fadd2(acc1, pk2(p0, p1));
+          else
+            acc0 = fadd2(acc0, pk2(p0, p1));
           pk[c] = pack_bf16x2(p0, p1);
         }
-        l += rs0 + rs1;
+        {
+          float a0, a1, a2, a3;
+          up2(acc0, a0, a1);
+          up2(acc1, a2, a3);
+          l += (a0 + a1) + (a2 + a3);
+        }
         tmem_st32(s_addr + 0, pk);
         tmem_st32(s_addr + 32, pk + 32);
         if (__any_sync(0xffffffffu, rescale)) {
           // O_i holds the complete sum through tile j-1: S_i(j) was issued
           // after P_i(j-1) V and its commit has fired.  Rows of this warp that
           // keep their maximum scale by 1.
+          const uint64_t alpha2 = pk2(alpha, alpha);
 #pragma unroll
           for (int c = 0; c < D; c += 32) {
             uint32_t r[32];
             tmem_ld32(o_addr + c, r);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            for (int e = 0; e < 32; e += 2) {
+              float a0, a1;
+              up2(fmul2(pk2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), alpha2), a0, a1);
+              r[e] = __float_as_uint(a0);
+              r[e + 1] = __float_as_uint(a1);
+            }
             tmem_st32(o_addr + c, r);
           }
         }
@@ -550,10 +666,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (ok) ok = warp_wait(bar_o[i], 0, limit, abort_flag, 8);
       if (ok) {
+        // Epilogue: O / l -> bf16 into this tile's Q buffer (free: every
+        // S_i MMA has completed) in the 128-byte-swizzled layout of the TMA
+        // box, then one TMA store per 64-column chunk.  Rows past Nq are
+        // clipped by the tensor map.
         tc_fence_after();
-        const int q = q0 + i * BM + wq * 32 + lane;
+        const int row = wq * 32 + lane;  // row of the 128-row tile
         const float inv_l = 1.f / l;
-        __nv_bfloat16* orow = p.out + ((static_cast<size_t>(b) * p.Nq + q) * p.H + h) * D;
+        const uint64_t inv2 = pk2(inv_l, inv_l);
+        uint8_t* qtile = base + C::Q_OFF + i * C::TILE_BYTES;
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
           uint32_t r[32];
@@ -561,15 +682,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_wait_ld();
           uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            w[e] = pack_bf16x2(__uint_as_float(r[2 * e]) * inv_l,
-                               __uint_as_float(r[2 * e + 1]) * inv_l);
-          if (q < p.Nq) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c);
-#pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+          for (int e = 0; e < 16; ++e) {
+            float a0, a1;
+            up2(fmul2(pk2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])), inv2),
+                a0, a1);
+            w[e] = pack_bf16x2(a0, a1);
           }
+          // Columns [c, c + 32) = 64 bytes = four 16-byte units of the
+          // 128-byte row of chunk c / 64.
+          uint8_t* chunk = qtile + (c / 64) * C::CHUNK_BYTES + row * 128;
+#pragma unroll
+          for (int u4 = 0; u4 < 4; ++u4) {
+            const int unit = ((c % 64) / 8) + u4;
+            *reinterpret_cast<uint4*>(chunk + ((unit ^ (row & 7)) << 4)) =
+                make_uint4(w[4 * u4], w[4 * u4 + 1], w[4 * u4 + 2], w[4 * u4 + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+        named_barrier(1 + i, 128);
+        if (wq == 0 && lane == 0) {
+          const uint32_t qt = qs + i * C::TILE_BYTES;
+          for (int c = 0; c < C::CHUNKS; ++c)
+            tma_store_4d(&p.tm_o, qt + c * C::CHUNK_BYTES, c * 64, h, q0 + i * BM, b);
+          tma_store_commit_and_drain();
         }
       }
     }
@@ -583,6 +718,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                  "r"(TMEM_COLS)
                  : "memory");
   }
+}
+
+// Test probe of the two exp2 paths the softmax uses: mode 0 the FMA-pipe
+// polynomial, mode 1 the MUFU ex2.approx.  One thread per pair of elements.
+__global__ void exp2_probe_kernel(const float* __restrict__ x, float* __restrict__ y, long long n,
+                                  int mode) {
+  const long long k = 2 * (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x);
+  if (k >= n) return;
+  const bool pair = k + 1 < n;
+  const float a = x[k];
+  const float b = pair ? x[k + 1] : 0.f;
+  float y0, y1;
+  if (mode == 0) {
+    exp2_poly2(pk2(a, b), y0, y1);
+  } else {
+    y0 = ex2(a);
+    y1 = ex2(b);
+  }
+  y[k] = y0;
+  if (pair) y[k + 1] = y1;
 }
 
 }  // namespace ncp
@@ -688,7 +843,7 @@ int run(const void* q, const void* kp, const void* vp, const void* kc, const voi
     prm.tm_k[0] = prm.tm_k[1];
     prm.tm_v[0] = prm.tm_v[1];
   }
-  prm.out = static_cast<__nv_bfloat16*>(out);
+  if (!make_map(&prm.tm_o, out, B, Nq, H, D)) return ATTN_ERR_CUDA;
   prm.Nq = Nq;
   prm.H = H;
   prm.n_tok[0] = Np;
@@ -747,6 +902,17 @@ int attn_device_status(cudaStream_t stream, unsigned int* info) {
     return ATTN_ERR_CUDA;
   if (info) *info = inf;
   return ATTN_ERR_TIMEOUT;
+}
+
+int attn_debug_exp2(const float* x, float* y, long long n, int mode, cudaStream_t stream) {
+  if (n < 0 || (mode != 0 && mode != 1)) return ATTN_ERR_SHAPE;
+  if (n == 0) return ATTN_OK;
+  if (!x || !y) return ATTN_ERR_NULL;
+  const long long pairs = (n + 1) / 2;
+  const long long blocks = (pairs + 255) / 256;
+  if (blocks > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+  ncp::exp2_probe_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, y, n, mode);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int attn_debug_set_fault(int mode, unsigned int wait_limit_us) {
