@@ -106,10 +106,15 @@ class ClockSampler:
             self.gpu_id = None
         self.proc = None
         self.lines = []
+        self.window = None
+
+    def mark(self, t0: float, t1: float):
+        """Host wall-clock bounds of the timed region."""
+        self.window = (t0, t1)
 
     def start(self):
         cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-               "-lms", "100"]
+               "-lms", "50"]
         if self.gpu_id:
             cmd.insert(1, f"--id={self.gpu_id}")
         try:
@@ -138,7 +143,22 @@ class ClockSampler:
         self.thread.join(timeout=2)
         sm, mx, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for _, line in self.lines:
+        lines = self.lines
+        in_window = 0
+        if self.window is not None and lines:
+            t0, t1 = self.window
+            # nvidia-smi prints a sample shortly after taking it: allow 0.1 s of lag.
+            inside = [(t, x) for t, x in lines if t0 <= t <= t1 + 0.1]
+            in_window = len(inside)
+            if inside:
+                lines = inside
+            else:
+                # The timed region was shorter than the sampling period: keep
+                # the samples nearest to it (same kernel, taken during the
+                # warm-up just before and the runs just after).
+                mid = 0.5 * (t0 + t1)
+                lines = sorted(lines, key=lambda tx: abs(tx[0] - mid))[:4]
+        for _, line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 8:
                 continue
@@ -154,8 +174,26 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm),
+                "reasons": sorted(reasons), "samples": len(sm), "samples_in_timed_region": in_window,
                 "power_w_max": max(power) if power else None}
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Maximum of ``value`` over the ranks of the default process group (the
+    value itself when there is no group or a single rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, steps: int, flops_per_step: int, slowest_ms: float) -> float:
+    """Whole-job TFLOP/s: every rank runs ``steps`` steps of its own replica;
+    the job takes as long as the slowest rank."""
+    return world * steps * flops_per_step / (slowest_ms / 1e3) / 1e12
 
 
 # ----------------------------------------------------------------------------
@@ -180,6 +218,7 @@ def time_device(torch, call, flush, steps, warmup, stream):
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t0 = time.time()
     with torch.cuda.stream(stream):
         for i in range(steps):
             flush.add_(1)
@@ -187,36 +226,56 @@ def time_device(torch, call, flush, steps, warmup, stream):
             call(stream)
             ends[i].record(stream)
     torch.cuda.synchronize()
-    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    t1 = time.time()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)], (t0, t1)
 
 
 def time_e2e(torch, ncp, w, host_in, steps, warmup, stream):
-    """Host-to-host time per call: pinned host inputs copied in, the C-ABI
-    call, the output copied back, all inside the CUDA-event region."""
-    dev_in = [torch.empty_like(t, device="cuda") for t in host_in]
-    dev_out = torch.empty_like(dev_in[0])
-    host_out = torch.empty_like(host_in[0]).pin_memory()
-    call = make_call(ncp, w, dev_in, dev_out)
+    """Host-to-host time per step through the C-ABI call: every step copies its
+    inputs in from pinned host memory, runs the call and copies the output back
+    to pinned host memory.  Two buffer sets and three streams (copies in,
+    compute, copies out) let step i's compute overlap step i+1's input copy and
+    step i-1's output copy, as a serving loop would; the CUDA events bracket
+    all ``steps`` steps, copies included."""
+    nbuf = 2
+    h2d_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
+    dev_in = [[torch.empty_like(t, device="cuda") for t in host_in] for _ in range(nbuf)]
+    dev_out = [torch.empty_like(dev_in[0][0]) for _ in range(nbuf)]
+    host_out = [torch.empty_like(host_in[0]).pin_memory() for _ in range(nbuf)]
+    calls = [make_call(ncp, w, dev_in[i], dev_out[i]) for i in range(nbuf)]
+    in_ready = [torch.cuda.Event() for _ in range(nbuf)]
+    computed = [torch.cuda.Event() for _ in range(nbuf)]
+    out_done = [torch.cuda.Event() for _ in range(nbuf)]
 
-    def one():
-        for d, h in zip(dev_in, host_in):
-            d.copy_(h, non_blocking=True)
-        call(stream)
-        host_out.copy_(dev_out, non_blocking=True)
+    def one(step):
+        i = step % nbuf
+        with torch.cuda.stream(h2d_stream):
+            h2d_stream.wait_event(computed[i])      # inputs of step - nbuf consumed
+            for d, h in zip(dev_in[i], host_in):
+                d.copy_(h, non_blocking=True)
+            in_ready[i].record(h2d_stream)
+        stream.wait_event(in_ready[i])
+        stream.wait_event(out_done[i])              # output of step - nbuf copied out
+        calls[i](stream)
+        computed[i].record(stream)
+        with torch.cuda.stream(d2h_stream):
+            d2h_stream.wait_event(computed[i])
+            host_out[i].copy_(dev_out[i], non_blocking=True)
+            out_done[i].record(d2h_stream)
 
-    with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            one()
-        torch.cuda.synchronize()
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
-        start.record(stream)
-        for _ in range(steps):
-            one()
-        end.record(stream)
+    for s in range(warmup):
+        one(s)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(h2d_stream)
+    for s in range(steps):
+        one(s)
+    d2h_stream.wait_event(computed[(steps - 1) % nbuf])
+    end.record(d2h_stream)
     torch.cuda.synchronize()
     h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = host_out.numel() * host_out.element_size()
+    d2h = host_out[0].numel() * host_out[0].element_size()
     return start.elapsed_time(end) / steps, h2d, d2h
 
 
@@ -280,31 +339,25 @@ def run_gpu(args):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    times = time_device(torch, call, flush, args.steps, args.warmup, stream)
+    times, window = time_device(torch, call, flush, args.steps, args.warmup, stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    clock_info = clocks.stop()
+    clocks.mark(*window)
     status, _ = ncp.device_status(stream)
     if status != ncp.ATTN_OK:
         raise RuntimeError(f"device status after timing: {ncp.status_string(status)}")
 
-    total_ms = sum(times)
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * args.steps * w.flops / (total_ms / 1e3) / 1e12
+    total_ms = max_over_ranks(sum(times), device="cuda")
+    value = job_throughput(world, args.steps, w.flops, total_ms)
     ms_per_step = total_ms / args.steps
 
     # End to end through the public API with host buffers.
     host_pinned = [t.pin_memory() for t in host_in]
-    e2e_ms, h2d, d2h = time_e2e(torch, ncp, w, host_pinned, max(3, args.steps // 2), 2, stream)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * w.flops / (e2e_ms / 1e3) / 1e12
+    e2e_ms, h2d, d2h = time_e2e(torch, ncp, w, host_pinned, max(4, args.steps), 3, stream)
+    e2e_ms = max_over_ranks(e2e_ms, device="cuda")
+    e2e_value = job_throughput(world, 1, w.flops, e2e_ms)
+    clock_info = clocks.stop()
 
     peaks, peak_src = measured_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
@@ -364,7 +417,7 @@ def per_config(torch, ncp, flush, stream, peak, args):
         out = torch.empty_like(dev_in[0])
         call = make_call(ncp, w, dev_in, out)
         steps = max(3, min(args.steps, 20))
-        times = time_device(torch, call, flush, steps, 3, stream)
+        times, _ = time_device(torch, call, flush, steps, 3, stream)
         us = statistics.median(times) * 1e3
         tf = w.flops / (us / 1e6) / 1e12
         res[w.name] = {"median_us": round(us, 2), "tflops": round(tf, 1),

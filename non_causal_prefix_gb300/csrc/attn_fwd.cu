@@ -26,7 +26,9 @@
 #include <stdint.h>
 
 #include <cmath>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "ncp_attn.h"
 
@@ -47,6 +49,20 @@ constexpr int MAX_SLOTS = 8;
 // the same maximum as the accumulated O, and p <= 2^8 stays far from overflow.
 constexpr float RESCALE_THRESHOLD = 8.0f;
 
+// Polynomial share of the exponentials (compile-time; overridable with -D).
+#ifndef NCP_POLY_NUM_D128
+#define NCP_POLY_NUM_D128 0
+#endif
+#ifndef NCP_POLY_DEN_D128
+#define NCP_POLY_DEN_D128 4
+#endif
+#ifndef NCP_POLY_NUM_D64
+#define NCP_POLY_NUM_D64 0
+#endif
+#ifndef NCP_POLY_DEN_D64
+#define NCP_POLY_DEN_D64 4
+#endif
+
 template <int D>
 struct Cfg {
   static constexpr int CHUNKS = D / 64;                  // 128-byte swizzle columns per row
@@ -61,19 +77,25 @@ struct Cfg {
   // the MUFU unit: POLY_NUM of every POLY_DEN packed pairs.  The MUFU unit does
   // 16 exp2 per clock per SM, as many as the S and P V MMAs need at D = 128;
   // at D = 64 the MMAs need half the time, so more moves to the polynomial.
-  static constexpr int POLY_NUM = (D == 128) ? 1 : 1;
-  static constexpr int POLY_DEN = (D == 128) ? 4 : 2;
+  static constexpr int POLY_NUM = (D == 128) ? NCP_POLY_NUM_D128 : NCP_POLY_NUM_D64;
+  static constexpr int POLY_DEN = (D == 128) ? NCP_POLY_DEN_D128 : NCP_POLY_DEN_D64;
+  static_assert(POLY_DEN >= 1 && POLY_NUM >= 0 && POLY_NUM <= POLY_DEN, "polynomial share");
   __host__ __device__ static constexpr bool poly_pair(int c) { return (c % POLY_DEN) >= POLY_DEN - POLY_NUM; }
 };
 
 struct SharedCtl {
   uint64_t q_full;
+  uint64_t q_free;
   uint64_t kv_full[MAX_SLOTS];
   uint64_t kv_empty[MAX_SLOTS];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_full[2];
+  uint64_t o_free[2];
+  uint64_t part_done[2];   // the 4 warps of a query tile wrote their partial rows
+  uint64_t merge_ready[2]; // the piece's arrival count is known (SharedCtl::last)
   uint64_t drain;
+  int last[2];             // this piece is the last of its unit: merge and store
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -82,8 +104,18 @@ struct Params {
   CUtensorMap tm_q;
   CUtensorMap tm_k[2];   // [0] prefix segment, [1] current segment
   CUtensorMap tm_v[2];
-  CUtensorMap tm_o;      // output, same box and swizzle as Q
+  __nv_bfloat16* out;
   int Nq, H;
+  int q_pairs;           // ceil(Nq / 256): units per (b, h); units are (b, h, q pair), q pair fastest
+  // Work items, walked round-robin by the persistent CTAs: items [0, n_whole)
+  // are whole units; the units of the last, partly filled round are cut into
+  // `pieces` key ranges each (items n_whole + r * pieces + k), merged through
+  // the workspace by whichever piece of a unit finishes last.
+  int n_items;
+  int n_whole;
+  int pieces;
+  float* ws_part;          // [split unit][piece][query tile][128 rows][D + 4]: O, m, l
+  unsigned int* ws_count;  // [split unit][query tile] finished pieces (reset by the merger)
   int n_tok[2];          // tokens per key segment
   int n_tiles[2];        // KV tiles per key segment
   float scale_log2;      // D^-0.5 * log2(e)
@@ -370,9 +402,154 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_
 }
 
 // ----------------------------------------------------------------------------
+// Work units and the softmax of one score tile
+// ----------------------------------------------------------------------------
+struct Unit {
+  int b, h, q0;
+  bool two;  // the second 128-row query tile has at least one row
+};
+
+__device__ __forceinline__ Unit decode_unit(const Params& p, int unit) {
+  Unit u;
+  const int qp = unit % p.q_pairs;
+  const int bh = unit / p.q_pairs;
+  u.h = bh % p.H;
+  u.b = bh / p.H;
+  u.q0 = qp * (2 * BM);
+  u.two = (u.q0 + BM) < p.Nq;
+  return u;
+}
+
+struct Item {
+  Unit u;
+  int t_begin, t_end;  // key tiles [t_begin, t_end) of the concatenated key sequence
+  int split;           // -1: whole unit; else index of the split unit
+  int piece;
+};
+
+__device__ __forceinline__ Item decode_item(const Params& p, int item, int T) {
+  Item it;
+  int unit;
+  if (item < p.n_whole) {
+    unit = item;
+    it.split = -1;
+    it.piece = 0;
+    it.t_begin = 0;
+    it.t_end = T;
+  } else {
+    const int r = (item - p.n_whole) / p.pieces;
+    const int k = (item - p.n_whole) % p.pieces;
+    unit = p.n_whole + r;
+    it.split = r;
+    it.piece = k;
+    it.t_begin = (k * T) / p.pieces;
+    it.t_end = ((k + 1) * T) / p.pieces;
+  }
+  it.u = decode_unit(p, unit);
+  return it;
+}
+
+// One 128-key tile of the online softmax for this thread's query row:
+// S (fp32, TMEM) -> running max m and sum l (log2 domain) -> P (bf16) written
+// over the first 64 columns of S; O is rescaled in TMEM when m moved.
+template <int D>
+__device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, int valid, float sl2,
+                                             bool may_rescale, float& m, float& l) {
+  float s[BN];
+  {
+    uint32_t r[BN];
+#pragma unroll
+    for (int c = 0; c < BN; c += 32) tmem_ld32(s_addr + c, r + c);
+    tmem_wait_ld();
+#pragma unroll
+    for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(r[c]);
+  }
+  if (valid < BN) {
+#pragma unroll
+    for (int c = 0; c < BN; ++c)
+      if (c >= valid) s[c] = -INFINITY;
+  }
+  // Row maximum: four independent chains of 3-input max.
+  float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
+  float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
+#pragma unroll
+  for (int c = 12; c + 8 <= BN; c += 8) {
+    mx0 = fmax3(mx0, s[c], s[c + 1]);
+    mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+    mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+    mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
+  }
+  mx0 = fmax3(mx0, s[BN - 4], s[BN - 3]);
+  mx1 = fmax3(mx1, s[BN - 2], s[BN - 1]);
+  const float m_tile = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
+  float alpha = 1.f;
+  bool rescale = false;
+  if (m_tile > m + RESCALE_THRESHOLD) {
+    alpha = ex2(m - m_tile);
+    l *= alpha;
+    m = m_tile;
+    rescale = may_rescale;
+  }
+  // p = 2^(s * scale * log2(e) - m) on packed pairs; pairs selected by
+  // poly_pair go through the FMA-pipe polynomial, the rest through MUFU.
+  const uint64_t sl2x2 = pk2(sl2, sl2);
+  const uint64_t neg_m2 = pk2(-m, -m);
+  uint64_t acc0 = 0, acc1 = 0;  // two packed running sums (bits 0 = 0.0f)
+  uint32_t pk[BN / 2];
+#pragma unroll
+  for (int c = 0; c < BN / 2; ++c) {
+    const uint64_t x = ffma2(pk2(s[2 * c], s[2 * c + 1]), sl2x2, neg_m2);
+    float p0, p1;
+    if (Cfg<D>::poly_pair(c)) {
+      exp2_poly2(x, p0, p1);
+    } else {
+      float x0, x1;
+      up2(x, x0, x1);
+      p0 = ex2(x0);
+      p1 = ex2(x1);
+    }
+    if (c & 1)
+      acc1 = fadd2(acc1, pk2(p0, p1));
+    else
+      acc0 = fadd2(acc0, pk2(p0, p1));
+    pk[c] = pack_bf16x2(p0, p1);
+  }
+  {
+    float a0, a1, a2, a3;
+    up2(acc0, a0, a1);
+    up2(acc1, a2, a3);
+    l += (a0 + a1) + (a2 + a3);
+  }
+  tmem_st32(s_addr + 0, pk);
+  tmem_st32(s_addr + 32, pk + 32);
+  if (__any_sync(0xffffffffu, rescale)) {
+    // O holds the complete sum through the previous tile: this S was issued
+    // after the previous P V and its commit has fired.  Rows of this warp
+    // that keep their maximum scale by 1.
+    const uint64_t alpha2 = pk2(alpha, alpha);
+#pragma unroll
+    for (int c = 0; c < D; c += 32) {
+      uint32_t r[32];
+      tmem_ld32(o_addr + c, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        float a0, a1;
+        up2(fmul2(pk2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), alpha2), a0, a1);
+        r[e] = __float_as_uint(a0);
+        r[e + 1] = __float_as_uint(a1);
+      }
+      tmem_st32(o_addr + c, r);
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
 // The kernel
 // ----------------------------------------------------------------------------
 template <int D>
+// 10 warps on 4 SM sub-partitions (16 Ki registers each, 3 warps on two of
+// them) cap a thread at 168 registers.
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ Params p) {
   using C = Cfg<D>;
@@ -386,33 +563,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int h = blockIdx.y;
-  const int b = blockIdx.z;
-  const int q0 = blockIdx.x * (2 * BM);
-  const bool two_tiles = (q0 + BM) < p.Nq;
   const int T0 = p.n_tiles[0];
   const int T = T0 + p.n_tiles[1];
   const uint64_t limit = p.wait_limit_ns;
+  const int n_items = p.n_items;
+  const int stride = static_cast<int>(gridDim.x);
 
   const uint32_t ring = base_u32 + C::RING_OFF;
   const uint32_t qs = base_u32 + C::Q_OFF;
   const uint32_t bar_q = smem_u32(&ctl->q_full);
+  const uint32_t bar_qfree = smem_u32(&ctl->q_free);
   auto bar_kv_full = [&](int s) { return smem_u32(&ctl->kv_full[s]); };
   auto bar_kv_empty = [&](int s) { return smem_u32(&ctl->kv_empty[s]); };
   const uint32_t bar_s[2] = {smem_u32(&ctl->s_full[0]), smem_u32(&ctl->s_full[1])};
   const uint32_t bar_p[2] = {smem_u32(&ctl->p_full[0]), smem_u32(&ctl->p_full[1])};
   const uint32_t bar_o[2] = {smem_u32(&ctl->o_full[0]), smem_u32(&ctl->o_full[1])};
+  const uint32_t bar_ofree[2] = {smem_u32(&ctl->o_free[0]), smem_u32(&ctl->o_free[1])};
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
+    mbar_init(bar_qfree, 1);
     for (int s = 0; s < C::NSLOT; ++s) {
       mbar_init(bar_kv_full(s), 1);
       mbar_init(bar_kv_empty(s), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_s[i], 1);
-      mbar_init(bar_p[i], 4);  // one arrival per softmax warp
+      mbar_init(bar_p[i], 4);      // one arrival per softmax warp
       mbar_init(bar_o[i], 1);
+      mbar_init(bar_ofree[i], 4);  // one arrival per softmax warp
+      mbar_init(smem_u32(&ctl->part_done[i]), 4);
+      mbar_init(smem_u32(&ctl->merge_ready[i]), 1);
     }
     mbar_init(smem_u32(&ctl->drain), 1);
     ctl->abort_flag = 0;
@@ -430,54 +611,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
+  // Loader bookkeeping for draining copies in flight after an abort.
+  uint32_t ld_issued = 0, ld_parity = 0;  // per ring slot: a load was issued / its phase
+  int q_last = -1;                        // last unit whose Q load was issued
 
   if (warp == PRODUCER_WARP) {
     // ---------------------------------------------------------------- loader
     if (lane == 0) {
       prefetch_tmap(&p.tm_q);
-      prefetch_tmap(&p.tm_o);
       for (int s = 0; s < 2; ++s) {
         prefetch_tmap(&p.tm_k[s]);
         prefetch_tmap(&p.tm_v[s]);
       }
-      const int nq_tiles = two_tiles ? 2 : 1;
-      mbar_expect_tx(bar_q, nq_tiles * C::TILE_BYTES);
-      for (int i = 0; i < nq_tiles; ++i)
-        for (int c = 0; c < C::CHUNKS; ++c)
-          tma_load_4d(qs + i * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tm_q, c * 64, h,
-                      q0 + i * BM, b, bar_q);
       int slot = 0;
       uint32_t phase = 0;
-      uint32_t issued = 0, issued_parity = 0;  // per slot: a load was issued / its phase
+      int n = 0;  // units done by this CTA
       bool ok = true;
-      for (int t = 0; t < T && ok; ++t) {
-        const int seg = (t < T0) ? 0 : 1;
-        const int tok0 = (t - (seg ? T0 : 0)) * BN;
-        for (int kind = 0; kind < 2; ++kind) {
-          ok = wait_bounded(bar_kv_empty(slot), phase ^ 1u, limit, abort_flag, 1);
+      for (int item = blockIdx.x; item < n_items && ok; item += stride, ++n) {
+        const Item it = decode_item(p, item, T);
+        const Unit& u = it.u;
+        // The Q buffers are free once every S MMA of the previous item is done.
+        if (n > 0) {
+          ok = wait_bounded(bar_qfree, (n - 1) & 1, limit, abort_flag, 9);
           if (!ok) break;
-          const bool skip = (p.fault_mode == 1) && kind == 1 && t == 1 && blockIdx.x == 0 &&
-                            blockIdx.y == 0 && blockIdx.z == 0;
-          if (!skip) {
-            const CUtensorMap* map = kind == 0 ? &p.tm_k[seg] : &p.tm_v[seg];
-            mbar_expect_tx(bar_kv_full(slot), C::TILE_BYTES);
-            for (int c = 0; c < C::CHUNKS; ++c)
-              tma_load_4d(ring + slot * C::TILE_BYTES + c * C::CHUNK_BYTES, map, c * 64, h, tok0,
-                          b, bar_kv_full(slot));
-            issued |= 1u << slot;
-            issued_parity = (issued_parity & ~(1u << slot)) | (phase << slot);
-          }
-          if (++slot == C::NSLOT) {
-            slot = 0;
-            phase ^= 1u;
+        }
+        const int nq_tiles = u.two ? 2 : 1;
+        mbar_expect_tx(bar_q, nq_tiles * C::TILE_BYTES);
+        for (int i = 0; i < nq_tiles; ++i)
+          for (int c = 0; c < C::CHUNKS; ++c)
+            tma_load_4d(qs + i * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tm_q, c * 64, u.h,
+                        u.q0 + i * BM, u.b, bar_q);
+        q_last = n;
+        for (int t = it.t_begin; t < it.t_end && ok; ++t) {
+          const int seg = (t < T0) ? 0 : 1;
+          const int tok0 = (t - (seg ? T0 : 0)) * BN;
+          for (int kind = 0; kind < 2; ++kind) {
+            ok = wait_bounded(bar_kv_empty(slot), phase ^ 1u, limit, abort_flag, 1);
+            if (!ok) break;
+            const bool skip = (p.fault_mode == 1) && kind == 1 && t == 1 && item == 0;
+            if (!skip) {
+              const CUtensorMap* map = kind == 0 ? &p.tm_k[seg] : &p.tm_v[seg];
+              mbar_expect_tx(bar_kv_full(slot), C::TILE_BYTES);
+              for (int c = 0; c < C::CHUNKS; ++c)
+                tma_load_4d(ring + slot * C::TILE_BYTES + c * C::CHUNK_BYTES, map, c * 64, u.h,
+                            tok0, u.b, bar_kv_full(slot));
+              ld_issued |= 1u << slot;
+              ld_parity = (ld_parity & ~(1u << slot)) | (phase << slot);
+            }
+            if (++slot == C::NSLOT) {
+              slot = 0;
+              phase ^= 1u;
+            }
           }
         }
-      }
-      if (!ok) {
-        // Abort: let every copy in flight land before the CTA exits.
-        wait_drain(bar_q, 0, limit);
-        for (int s = 0; s < C::NSLOT; ++s)
-          if (issued & (1u << s)) wait_drain(bar_kv_full(s), (issued_parity >> s) & 1u, limit);
       }
     }
     __syncwarp();
@@ -486,7 +672,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t IDESC_S = make_idesc(BM, BN, false);
       constexpr uint32_t IDESC_PV = make_idesc(BM, D, true);
-      const int nq = two_tiles ? 2 : 1;
       // S_i = Q_i K^T over D in K-steps of 16 (32 bytes inside a 128-byte row).
       auto issue_s = [&](int i, int k_slot) {
         const uint32_t qa = qs + i * C::TILE_BYTES;
@@ -508,47 +693,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                  (accumulate || kk > 0) ? 1u : 0u);
       };
 
-      bool ok = wait_bounded(bar_q, 0, limit, abort_flag, 2);
       int slot = 0;
       uint32_t phase = 0;
-      int v_prev = -1;
-      for (int j = 0; j < T && ok; ++j) {
-        const int k_slot = slot;
-        ok = wait_bounded(bar_kv_full(k_slot), phase, limit, abort_flag, 3);
-        if (!ok) break;
-        if (++slot == C::NSLOT) { slot = 0; phase ^= 1u; }
+      uint32_t sc[2] = {0u, 0u};  // S commits per query tile (phases of s_full / p_full)
+      uint32_t oc[2] = {0u, 0u};  // units finished per query tile (phases of o_full / o_free)
+      bool ok = true;
+      int n = 0;
+      // The first P V of a unit overwrites O_i: wait until the epilogue of the
+      // previous unit has read it out of TMEM.
+      auto pv = [&](int i, int v_slot, bool accumulate) -> bool {
+        if (!wait_bounded(bar_p[i], (sc[i] - 1u) & 1u, limit, abort_flag, 4)) return false;
+        if (!accumulate && oc[i] > 0 &&
+            !wait_bounded(bar_ofree[i], (oc[i] - 1u) & 1u, limit, abort_flag, 6))
+          return false;
         tc_fence_after();
-        for (int i = 0; i < nq && ok; ++i) {
-          if (j > 0) {
-            ok = wait_bounded(bar_p[i], (j - 1) & 1, limit, abort_flag, 4);
-            if (!ok) break;
-            tc_fence_after();
-            issue_pv(i, v_prev, j - 1 > 0);
+        issue_pv(i, v_slot, accumulate);
+        return true;
+      };
+      for (int item = blockIdx.x; item < n_items && ok; item += stride, ++n) {
+        const Item it = decode_item(p, item, T);
+        const int nq = it.u.two ? 2 : 1;
+        const int nt = it.t_end - it.t_begin;
+        ok = wait_bounded(bar_q, n & 1, limit, abort_flag, 2);
+        if (!ok) break;
+        int v_prev = -1;
+        for (int j = 0; j < nt && ok; ++j) {
+          const int k_slot = slot;
+          ok = wait_bounded(bar_kv_full(k_slot), phase, limit, abort_flag, 3);
+          if (!ok) break;
+          if (++slot == C::NSLOT) { slot = 0; phase ^= 1u; }
+          tc_fence_after();
+          for (int i = 0; i < nq && ok; ++i) {
+            if (j > 0) {
+              ok = pv(i, v_prev, j - 1 > 0);
+              if (!ok) break;
+            }
+            issue_s(i, k_slot);
+            mma_commit(bar_s[i]);
+            ++sc[i];
           }
-          issue_s(i, k_slot);
-          mma_commit(bar_s[i]);
+          if (!ok) break;
+          if (j > 0) mma_commit(bar_kv_empty(v_prev));
+          mma_commit(bar_kv_empty(k_slot));
+          const int v_slot = slot;
+          ok = wait_bounded(bar_kv_full(v_slot), phase, limit, abort_flag, 5);
+          if (!ok) break;
+          if (++slot == C::NSLOT) { slot = 0; phase ^= 1u; }
+          v_prev = v_slot;
         }
         if (!ok) break;
-        if (j > 0) mma_commit(bar_kv_empty(v_prev));
-        mma_commit(bar_kv_empty(k_slot));
-        const int v_slot = slot;
-        ok = wait_bounded(bar_kv_full(v_slot), phase, limit, abort_flag, 5);
-        if (!ok) break;
-        if (++slot == C::NSLOT) { slot = 0; phase ^= 1u; }
-        v_prev = v_slot;
-      }
-      for (int i = 0; i < nq && ok; ++i) {
-        ok = wait_bounded(bar_p[i], (T - 1) & 1, limit, abort_flag, 6);
-        if (!ok) break;
-        tc_fence_after();
-        issue_pv(i, v_prev, T - 1 > 0);
-        mma_commit(bar_o[i]);
-      }
-      if (ok) mma_commit(bar_kv_empty(v_prev));
-      if (!ok) {
-        // Abort: let every MMA in flight finish before TMEM is released.
-        mma_commit(smem_u32(&ctl->drain));
-        wait_drain(smem_u32(&ctl->drain), 0, limit);
+        mma_commit(bar_qfree);  // every S MMA of this item has been issued
+        for (int i = 0; i < nq && ok; ++i) {
+          ok = pv(i, v_prev, nt - 1 > 0);
+          if (!ok) break;
+          mma_commit(bar_o[i]);
+          ++oc[i];
+        }
+        if (ok) mma_commit(bar_kv_empty(v_prev));
       }
     }
     __syncwarp();
@@ -556,155 +757,129 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------- softmax / correction / store
     const int i = warp >> 2;  // query tile
     const int wq = warp & 3;  // TMEM lane quarter
-    if (i == 0 || two_tiles) {
-      const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-      const uint32_t s_addr = tmem + lane_base + tmem_s_col(i);
-      const uint32_t o_addr = tmem + lane_base + tmem_o_col(i);
-      const float sl2 = p.scale_log2;
-      const uint64_t sl2x2 = pk2(sl2, sl2);
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t s_addr = tmem + lane_base + tmem_s_col(i);
+    const uint32_t o_addr = tmem + lane_base + tmem_o_col(i);
+    const float sl2 = p.scale_log2;
+    uint32_t sc = 0, oc = 0;  // phases of s_full / p_full and of o_full / o_free
+    bool ok = true;
+    uint32_t mc = 0;  // split items done by this query tile (phases of part_done / merge_ready)
+    const uint32_t bar_part = smem_u32(&ctl->part_done[i]);
+    const uint32_t bar_merge = smem_u32(&ctl->merge_ready[i]);
+    const int row = wq * 32 + lane;  // row of the 128-row query tile (= TMEM lane)
+    for (int item = blockIdx.x; item < n_items && ok; item += stride) {
+      const Item it = decode_item(p, item, T);
+      const Unit& u = it.u;
+      if (i == 1 && !u.two) continue;
       float m = -INFINITY;  // running (possibly stale) maximum, log2 units
       float l = 0.f;        // running sum of exp2(x - m)
-      bool ok = true;
-      for (int j = 0; j < T; ++j) {
-        ok = warp_wait(bar_s[i], j & 1, limit, abort_flag, 7);
+      for (int t = it.t_begin; t < it.t_end; ++t) {
+        ok = warp_wait(bar_s[i], sc & 1u, limit, abort_flag, 7);
         if (!ok) break;
+        ++sc;
         tc_fence_after();
-        float s[BN];
-        {
-          uint32_t r[BN];
-#pragma unroll
-          for (int c = 0; c < BN; c += 32) tmem_ld32(s_addr + c, r + c);
-          tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(r[c]);
-        }
         // Keys past the end of this segment: TMA filled them with zeros, their
         // scores must be -inf instead.
-        const int seg = (j < T0) ? 0 : 1;
-        const int valid = p.n_tok[seg] - (j - (seg ? T0 : 0)) * BN;
-        if (valid < BN) {
-#pragma unroll
-          for (int c = 0; c < BN; ++c)
-            if (c >= valid) s[c] = -INFINITY;
-        }
-        // Row maximum: four independent chains of 3-input max.
-        float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
-        float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
-#pragma unroll
-        for (int c = 12; c + 8 <= BN; c += 8) {
-          mx0 = fmax3(mx0, s[c], s[c + 1]);
-          mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
-          mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
-          mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
-        }
-        mx0 = fmax3(mx0, s[BN - 4], s[BN - 3]);
-        mx1 = fmax3(mx1, s[BN - 2], s[BN - 1]);
-        const float m_tile = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
-        float alpha = 1.f;
-        bool rescale = false;
-        if (m_tile > m + RESCALE_THRESHOLD) {
-          alpha = ex2(m - m_tile);
-          l *= alpha;
-          m = m_tile;
-          rescale = (j > 0);
-        }
-        // p = 2^(s * scale * log2(e) - m) on packed pairs; pairs selected by
-        // PolySel go through the FMA-pipe polynomial, the rest through MUFU.
-        const uint64_t neg_m2 = pk2(-m, -m);
-        uint64_t acc0 = 0, acc1 = 0;  // two packed running sums (bits 0 = 0.0f)
-        uint32_t pk[BN / 2];
-#pragma unroll
-        for (int c = 0; c < BN / 2; ++c) {
-          const uint64_t x = ffma2(pk2(s[2 * c], s[2 * c + 1]), sl2x2, neg_m2);
-          float p0, p1;
-          if (Cfg<D>::poly_pair(c)) {
-            exp2_poly2(x, p0, p1);
-          } else {
-            float x0, x1;
-            up2(x, x0, x1);
-            p0 = ex2(x0);
-            p1 = ex2(x1);
-          }
-          if (c & 1)
-            acc1 = fadd2(acc1, pk2(p0, p1));
-          else
-            acc0 = fadd2(acc0, pk2(p0, p1));
-          pk[c] = pack_bf16x2(p0, p1);
-        }
-        {
-          float a0, a1, a2, a3;
-          up2(acc0, a0, a1);
-          up2(acc1, a2, a3);
-          l += (a0 + a1) + (a2 + a3);
-        }
-        tmem_st32(s_addr + 0, pk);
-        tmem_st32(s_addr + 32, pk + 32);
-        if (__any_sync(0xffffffffu, rescale)) {
-          // O_i holds the complete sum through tile j-1: S_i(j) was issued
-          // after P_i(j-1) V and its commit has fired.  Rows of this warp that
-          // keep their maximum scale by 1.
-          const uint64_t alpha2 = pk2(alpha, alpha);
-#pragma unroll
-          for (int c = 0; c < D; c += 32) {
-            uint32_t r[32];
-            tmem_ld32(o_addr + c, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              float a0, a1;
-              up2(fmul2(pk2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), alpha2), a0, a1);
-              r[e] = __float_as_uint(a0);
-              r[e + 1] = __float_as_uint(a1);
-            }
-            tmem_st32(o_addr + c, r);
-          }
-        }
+        const int seg = (t < T0) ? 0 : 1;
+        const int valid = p.n_tok[seg] - (t - (seg ? T0 : 0)) * BN;
+        softmax_tile<D>(s_addr, o_addr, valid, sl2, t > it.t_begin, m, l);
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_p[i]);
       }
-      if (ok) ok = warp_wait(bar_o[i], 0, limit, abort_flag, 8);
-      if (ok) {
-        // Epilogue: O / l -> bf16 into this tile's Q buffer (free: every
-        // S_i MMA has completed) in the 128-byte-swizzled layout of the TMA
-        // box, then one TMA store per 64-column chunk.  Rows past Nq are
-        // clipped by the tensor map.
-        tc_fence_after();
-        const int row = wq * 32 + lane;  // row of the 128-row tile
+      if (!ok) break;
+      ok = warp_wait(bar_o[i], oc & 1u, limit, abort_flag, 8);
+      if (!ok) break;
+      ++oc;
+      tc_fence_after();
+      // Epilogue: read O_i out of TMEM and release it to the next item's P V.
+      uint32_t r[D];
+#pragma unroll
+      for (int c = 0; c < D; c += 32) tmem_ld32(o_addr + c, r + c);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_ofree[i]);
+
+      if (it.split >= 0) {
+        // A piece of a split unit: publish (O, m, l) of this row, count the
+        // piece in; the last piece of the unit merges every piece.
+        constexpr int RS = D + 4;  // row stride in floats (16-byte aligned)
+        const size_t tile_rows = static_cast<size_t>(2) * BM;
+        float* part_base = p.ws_part + static_cast<size_t>(it.split) * p.pieces * tile_rows * RS;
+        auto part_row = [&](int k) {
+          return part_base + ((static_cast<size_t>(k) * 2 + i) * BM + row) * RS;
+        };
+        {
+          float4* dst = reinterpret_cast<float4*>(part_row(it.piece));
+#pragma unroll
+          for (int c = 0; c < D; c += 4)
+            __stcg(dst + c / 4, make_float4(__uint_as_float(r[c]), __uint_as_float(r[c + 1]),
+                                            __uint_as_float(r[c + 2]), __uint_as_float(r[c + 3])));
+          __stcg(dst + D / 4, make_float4(m, l, 0.f, 0.f));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_part);
+        if (wq == 0 && lane == 0) {
+          ok = wait_bounded(bar_part, mc & 1u, limit, abort_flag, 10);
+          if (ok) {
+            __threadfence();
+            const unsigned int before = atomicAdd(p.ws_count + it.split * 2 + i, 1u);
+            const int last = before == static_cast<unsigned int>(p.pieces - 1);
+            if (last) {
+              __threadfence();
+              atomicExch(p.ws_count + it.split * 2 + i, 0u);  // ready for the next launch
+            }
+            ctl->last[i] = last;
+            mbar_arrive(bar_merge);
+          }
+        }
+        ok = warp_wait(bar_merge, mc & 1u, limit, abort_flag, 11);
+        ++mc;
+        if (!ok) break;
+        if (!*reinterpret_cast<volatile int*>(&ctl->last[i])) continue;
+        // Merge every piece (this one's included, read back) in piece order,
+        // so the result does not depend on which piece finished last.
+        float m_all = -INFINITY;
+        for (int k = 0; k < p.pieces; ++k) m_all = fmaxf(m_all, __ldcg(part_row(k) + D));
+        l = 0.f;
+#pragma unroll
+        for (int c = 0; c < D; ++c) r[c] = 0u;
+        for (int k = 0; k < p.pieces; ++k) {
+          const float4* src4 = reinterpret_cast<const float4*>(part_row(k));
+          const float4 ml = __ldcg(src4 + D / 4);
+          const float a = ex2(ml.x - m_all);
+          l = fmaf(ml.y, a, l);
+#pragma unroll
+          for (int c = 0; c < D; c += 4) {
+            const float4 v = __ldcg(src4 + c / 4);
+            r[c] = __float_as_uint(fmaf(v.x, a, __uint_as_float(r[c])));
+            r[c + 1] = __float_as_uint(fmaf(v.y, a, __uint_as_float(r[c + 1])));
+            r[c + 2] = __float_as_uint(fmaf(v.z, a, __uint_as_float(r[c + 2])));
+            r[c + 3] = __float_as_uint(fmaf(v.w, a, __uint_as_float(r[c + 3])));
+          }
+        }
+      }
+
+      // O / l -> bf16 -> this thread's output row.
+      const int q = u.q0 + i * BM + row;
+      if (q < p.Nq) {
         const float inv_l = 1.f / l;
         const uint64_t inv2 = pk2(inv_l, inv_l);
-        uint8_t* qtile = base + C::Q_OFF + i * C::TILE_BYTES;
+        uint4* dst = reinterpret_cast<uint4*>(
+            p.out + ((static_cast<size_t>(u.b) * p.Nq + q) * p.H + u.h) * D);
 #pragma unroll
-        for (int c = 0; c < D; c += 32) {
-          uint32_t r[32];
-          tmem_ld32(o_addr + c, r);
-          tmem_wait_ld();
-          uint32_t w[16];
+        for (int c = 0; c < D; c += 8) {
+          uint32_t w[4];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
+          for (int e = 0; e < 4; ++e) {
             float a0, a1;
-            up2(fmul2(pk2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])), inv2),
+            up2(fmul2(pk2(__uint_as_float(r[c + 2 * e]), __uint_as_float(r[c + 2 * e + 1])), inv2),
                 a0, a1);
             w[e] = pack_bf16x2(a0, a1);
           }
-          // Columns [c, c + 32) = 64 bytes = four 16-byte units of the
-          // 128-byte row of chunk c / 64.
-          uint8_t* chunk = qtile + (c / 64) * C::CHUNK_BYTES + row * 128;
-#pragma unroll
-          for (int u4 = 0; u4 < 4; ++u4) {
-            const int unit = ((c % 64) / 8) + u4;
-            *reinterpret_cast<uint4*>(chunk + ((unit ^ (row & 7)) << 4)) =
-                make_uint4(w[4 * u4], w[4 * u4 + 1], w[4 * u4 + 2], w[4 * u4 + 3]);
-          }
-        }
-        fence_proxy_async_smem();
-        named_barrier(1 + i, 128);
-        if (wq == 0 && lane == 0) {
-          const uint32_t qt = qs + i * C::TILE_BYTES;
-          for (int c = 0; c < C::CHUNKS; ++c)
-            tma_store_4d(&p.tm_o, qt + c * C::CHUNK_BYTES, c * 64, h, q0 + i * BM, b);
-          tma_store_commit_and_drain();
+          dst[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
     }
@@ -712,6 +887,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (*abort_flag) {
+    // Some role gave up: before the CTA exits and TMEM is released, let every
+    // TMA copy and every MMA still in flight land (bounded waits again).
+    if (warp == PRODUCER_WARP && lane == 0) {
+      if (q_last >= 0) wait_drain(bar_q, q_last & 1, limit);
+      for (int s = 0; s < C::NSLOT; ++s)
+        if (ld_issued & (1u << s)) wait_drain(bar_kv_full(s), (ld_parity >> s) & 1u, limit);
+    }
+    if (warp == MMA_WARP && lane == 0) {
+      mma_commit(smem_u32(&ctl->drain));
+      wait_drain(smem_u32(&ctl->drain), 0, limit);
+    }
+    __syncwarp();
+  }
   if (warp == MMA_WARP) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -796,20 +985,100 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
+// ---------------------------------------------------------------------------
+// Split workspace: partial (O, m, l) rows of the pieces of split units plus one
+// arrival counter per (split unit, query tile).  One per (device, stream), so
+// calls that run concurrently on different streams never share one; created on
+// the first call that splits (cudaMalloc, then a zeroing memset on that
+// stream) and kept until the process exits.
+// ---------------------------------------------------------------------------
+constexpr int MAX_PIECES = 8;
+// A piece pays a Q load, a pipeline fill and a partial write + merge: give it
+// at least this many key tiles.
+constexpr int MIN_PIECE_TILES = 4;
+
+struct Workspace {
+  float* part = nullptr;
+  unsigned int* count = nullptr;
+};
+
+std::mutex g_ws_mutex;
+std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
+
+// Piece slots = SM count (a split schedule never has more pieces than CTAs).
+size_t ws_part_bytes(int sms) {
+  return static_cast<size_t>(sms) * 2 * ncp::BM * (128 + 4) * sizeof(float);
+}
+
+const Workspace* get_workspace(int dev, int sms, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  const auto key = std::make_pair(dev, reinterpret_cast<uintptr_t>(stream));
+  auto found = g_ws.find(key);
+  if (found != g_ws.end()) return &found->second;
+  // Allocation is not allowed while the stream is being captured into a graph:
+  // then the call runs without splitting.
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  Workspace ws;
+  const size_t count_bytes = static_cast<size_t>(2) * sms * sizeof(unsigned int);
+  if (cudaMalloc(reinterpret_cast<void**>(&ws.part), ws_part_bytes(sms)) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (cudaMalloc(reinterpret_cast<void**>(&ws.count), count_bytes) != cudaSuccess ||
+      cudaMemsetAsync(ws.count, 0, count_bytes, stream) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(ws.part);
+    if (ws.count) cudaFree(ws.count);
+    return nullptr;
+  }
+  return &(g_ws[key] = ws);
+}
+
 template <int D>
-int launch(Params& prm, int B, int Nq, int H, cudaStream_t stream) {
+int launch(Params& prm, long long n_units, cudaStream_t stream) {
   using C = ncp::Cfg<D>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
-  static bool configured[64] = {};
+  static int sm_count[64] = {};  // per device, 0 = not configured yet
   if (dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
-  if (!configured[dev]) {
+  if (sm_count[dev] == 0) {
+    int sms = 0;
     if (cudaFuncSetAttribute(ncp::attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_BYTES) != cudaSuccess)
+                             C::SMEM_BYTES) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms < 1)
       return ATTN_ERR_CUDA;
-    configured[dev] = true;
+    sm_count[dev] = sms;
   }
-  const dim3 grid((Nq + 2 * ncp::BM - 1) / (2 * ncp::BM), H, B);
+  const int sms = sm_count[dev];
+  // Schedule.  Whole units fill complete rounds of `sms` persistent CTAs; the
+  // units of the last, partly filled round are cut into `pieces` key ranges
+  // each so that round keeps (nearly) every SM busy.
+  const int T = prm.n_tiles[0] + prm.n_tiles[1];
+  const long long rem = n_units % sms;
+  long long pieces = 1;
+  if (rem > 0) {
+    pieces = sms / rem;
+    if (pieces > T / MIN_PIECE_TILES) pieces = T / MIN_PIECE_TILES;
+    if (pieces > MAX_PIECES) pieces = MAX_PIECES;
+  }
+  const Workspace* ws = pieces >= 2 ? get_workspace(dev, sms, stream) : nullptr;
+  if (!ws) pieces = 1;
+  const long long n_whole = pieces >= 2 ? n_units - rem : n_units;
+  const long long n_items = n_whole + (n_units - n_whole) * pieces;
+  if (n_items > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+  prm.n_whole = static_cast<int>(n_whole);
+  prm.n_items = static_cast<int>(n_items);
+  prm.pieces = static_cast<int>(pieces);
+  prm.ws_part = ws ? ws->part : nullptr;
+  prm.ws_count = ws ? ws->count : nullptr;
+  // Persistent grid: one CTA per SM (shared memory and TMEM allow one), each
+  // walking the items round-robin.
+  const int grid = n_items < sms ? static_cast<int>(n_items) : sms;
   ncp::attn_fwd_kernel<D><<<grid, ncp::NUM_THREADS, C::SMEM_BYTES, stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -843,9 +1112,13 @@ int run(const void* q, const void* kp, const void* vp, const void* kc, const voi
     prm.tm_k[0] = prm.tm_k[1];
     prm.tm_v[0] = prm.tm_v[1];
   }
-  if (!make_map(&prm.tm_o, out, B, Nq, H, D)) return ATTN_ERR_CUDA;
+  const long long q_pairs = (static_cast<long long>(Nq) + 2 * ncp::BM - 1) / (2 * ncp::BM);
+  const long long n_units = static_cast<long long>(B) * H * q_pairs;
+  if (n_units > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+  prm.out = static_cast<__nv_bfloat16*>(out);
   prm.Nq = Nq;
   prm.H = H;
+  prm.q_pairs = static_cast<int>(q_pairs);
   prm.n_tok[0] = Np;
   prm.n_tok[1] = Nc;
   prm.n_tiles[0] = (Np + ncp::BN - 1) / ncp::BN;
@@ -856,7 +1129,7 @@ int run(const void* q, const void* kp, const void* vp, const void* kc, const voi
     prm.fault_mode = g_fault_mode;
     prm.wait_limit_ns = g_wait_limit_ns;
   }
-  return D == 128 ? launch<128>(prm, B, Nq, H, stream) : launch<64>(prm, B, Nq, H, stream);
+  return D == 128 ? launch<128>(prm, n_units, stream) : launch<64>(prm, n_units, stream);
 }
 
 }  // namespace

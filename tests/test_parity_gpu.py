@@ -82,6 +82,61 @@ def test_prefix_small(cuda_lib, oracle_mod, B, Nq, Np, Nc, H, D):
     assert_parity(f64(out), ref, g.describe())
 
 
+# Shapes with fewer work units than SMs and many key tiles: the last (here the
+# only) round of units is cut into key-range pieces merged through the
+# workspace.  The prefix case cuts across the prefix/current boundary.
+SPLIT_CASES = [  # (kind, B, Nq, Np, Nc, H, D)
+    ("dense", 1, 2048, 0, 2048, 3, 128), ("dense", 1, 4096, 0, 4096, 1, 64),
+    ("dense", 2, 1000, 0, 1000, 1, 128), ("prefix", 1, 512, 640, 512, 2, 128),
+    ("prefix", 1, 200, 1100, 300, 2, 64),
+]
+
+
+def split_inputs(kind, B, Nq, Np, Nc, H, D, seed):
+    shapes = [(B, Nq, H, D)]
+    if kind == "prefix":
+        shapes += [(B, Np, H, D)] * 2
+    shapes += [(B, Nc, H, D)] * 2
+    return [workloads.randn_bf16(s, 1.0, seed + i) for i, s in enumerate(shapes)]
+
+
+def run_split(ncp, kind, dev):
+    if kind == "dense":
+        return gpu_dense(ncp, *dev)
+    return gpu_prefix(ncp, *dev)
+
+
+@pytest.mark.parametrize("case", SPLIT_CASES)
+def test_split_units(cuda_lib, oracle_mod, case):
+    kind, B, Nq, Np, Nc, H, D = case
+    ins = split_inputs(kind, B, Nq, Np, Nc, H, D, 9900 + Nq + Np)
+    out = run_split(cuda_lib, kind, to_dev(ins))
+    if kind == "dense":
+        ref = oracle_mod.dense_attention(*bits(ins))
+    else:
+        ref = oracle_mod.prefix_attention(*bits(ins))
+    assert_parity(f64(out), ref, str(case))
+
+
+def test_split_units_deterministic_and_per_stream(cuda_lib):
+    """The merge sums the pieces in a fixed order: repeated calls are
+    bit-identical; calls on two streams at once use separate workspaces."""
+    kind, B, Nq, Np, Nc, H, D = SPLIT_CASES[0]
+    ins = to_dev(split_inputs(kind, B, Nq, Np, Nc, H, D, 9950))
+    first = run_split(cuda_lib, kind, ins)
+    for _ in range(3):
+        assert torch.equal(run_split(cuda_lib, kind, ins), first)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [torch.empty_like(ins[0]) for _ in streams]
+    torch.cuda.synchronize()
+    for _ in range(4):
+        for s, o in zip(streams, outs):
+            cuda_lib.attn_dense_fwd(*ins, o, stream=s)
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(o, first)
+
+
 def test_prefix_equals_concat_bitwise(cuda_lib):
     """With Np a multiple of the 128-key tile, walking the two segments visits
     the same tiles in the same order as one concatenated key set, so the
