@@ -76,6 +76,28 @@ int attn_prefix_fwd(const void *q, const void *kp, const void *vp, const void *k
                     const void *vc, void *out, int B, int Nq, int Np, int Nc, int H, int D,
                     cudaStream_t stream);
 
+/*
+ * attn_dense_fwd without any allocation, for callers that cannot call
+ * cudaMalloc: an engine whose memory pool already owns the device memory, a
+ * plugin that is handed only its input and output buffers, or a latency-bound
+ * loop that cannot afford an allocation's implicit device synchronisation.
+ * The pages define no such call; it is a deployment variant of the dense form.
+ *
+ * Same arguments, result and errors as attn_dense_fwd.  The split workspace
+ * (partial rows of key-range pieces and their arrival counters) lives in one
+ * static device array of 21.6 MB (160 pieces at D <= 128) that every GPU
+ * loading this library holds until the process exits; no cudaMalloc, no
+ * cudaFree.  A call whose schedule needs more pieces than that (only on a GPU
+ * with more than 160 SMs) returns ATTN_ERR_SHAPE and launches nothing.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call clears the counters on `stream`, then uses the array: calls
+ * that overlap on the GPU (other streams, other host threads) race on it and
+ * must be serialised by the caller.
+ */
+int attn_dense_fwd_noalloc(const void *q, const void *k, const void *v, void *out,
+                           int B, int N, int H, int D, cudaStream_t stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char *attn_status_string(int status);
 

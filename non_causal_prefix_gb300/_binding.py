@@ -30,6 +30,7 @@ SIGNATURES = {
     "attn_device_status": (_I, [_VP, _UIP]),
     "attn_debug_set_fault": (_I, [_I, ctypes.c_uint]),
     "attn_debug_exp2": (_I, [_VP, _VP, ctypes.c_longlong, _I, _VP]),
+    "attn_dense_fwd_noalloc": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
 }
 
 _lock = threading.Lock()
@@ -100,6 +101,20 @@ def attn_dense_fwd(q, k, v, out, stream=None) -> None:
     rc = load_library().attn_dense_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                                        B, N, H, D, _stream_handle(stream))
     _check(rc, "attn_dense_fwd")
+
+
+def attn_dense_fwd_noalloc(q, k, v, out, stream=None) -> None:
+    """``attn_dense_fwd`` with its workspace in the library's static device
+    scratch instead of a cudaMalloc'd one (see the C header: calls that
+    overlap on the GPU race on that scratch)."""
+    B, N, H, D = _bnhd(q, "q")
+    for t, n in ((k, "k"), (v, "v"), (out, "out")):
+        if tuple(t.shape) != (B, N, H, D):
+            raise ValueError(f"{n} must have q's shape {tuple(q.shape)}")
+    _check_tensors(q, k, v, out)
+    rc = load_library().attn_dense_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                               out.data_ptr(), B, N, H, D, _stream_handle(stream))
+    _check(rc, "attn_dense_fwd_noalloc")
 
 
 def attn_prefix_fwd(q, kp, vp, kc, vc, out, stream=None) -> None:

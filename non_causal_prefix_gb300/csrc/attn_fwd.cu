@@ -932,6 +932,24 @@ __global__ void exp2_probe_kernel(const float* __restrict__ x, float* __restrict
 }  // namespace ncp
 
 // ============================================================================
+// Fixed scratch for attn_dense_fwd_noalloc: the split workspace (arrival
+// counters, then partial rows) of a call that may not allocate, as one static
+// device array.  Every GPU that loads this library holds it until the process
+// exits.  Sized for 160 pieces, one per SM of a GPU with up to 160 SMs, at
+// D <= 128: 256-byte aligned counter block, then 160 x 2 x 128 rows x
+// (128 + 4) floats.
+// ============================================================================
+namespace ncp {
+constexpr int NOALLOC_PIECES = 160;
+constexpr size_t NOALLOC_COUNT_BYTES = 2 * NOALLOC_PIECES * sizeof(unsigned int);  // 1280
+constexpr size_t NOALLOC_PART_BYTES =
+    static_cast<size_t>(NOALLOC_PIECES) * 2 * BM * (128 + 4) * sizeof(float);
+constexpr size_t NOALLOC_SCRATCH_BYTES = NOALLOC_COUNT_BYTES + NOALLOC_PART_BYTES;  // 21.6 MB
+static_assert(NOALLOC_COUNT_BYTES % 256 == 0, "partial rows start 256-byte aligned");
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
+}  // namespace ncp
+
+// ============================================================================
 // Host side: argument checks, TMA descriptors, launch
 // ============================================================================
 namespace {
@@ -1083,8 +1101,10 @@ int launch(Params& prm, long long n_units, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int run(const void* q, const void* kp, const void* vp, const void* kc, const void* vc, void* out,
-        int B, int Nq, int Np, int Nc, int H, int D, cudaStream_t stream) {
+// Argument checks, TMA descriptors and kernel parameters of one call.
+int prepare(const void* q, const void* kp, const void* vp, const void* kc, const void* vc,
+            void* out, int B, int Nq, int Np, int Nc, int H, int D, Params& prm,
+            long long& n_units) {
   if (!q || !kc || !vc || !out || (Np > 0 && (!kp || !vp))) return ATTN_ERR_NULL;
   if (B < 1 || Nq < 1 || Nc < 1 || H < 1 || Np < 0) return ATTN_ERR_SHAPE;
   if (H > 65535 || B > 65535) return ATTN_ERR_SHAPE;
@@ -1101,7 +1121,6 @@ int run(const void* q, const void* kp, const void* vp, const void* kc, const voi
       (Np > 0 && (overlaps(out, q_bytes, kp, p_bytes) || overlaps(out, q_bytes, vp, p_bytes))))
     return ATTN_ERR_ALIAS;
 
-  Params prm;
   if (!make_map(&prm.tm_q, q, B, Nq, H, D)) return ATTN_ERR_CUDA;
   if (!make_map(&prm.tm_k[1], kc, B, Nc, H, D) || !make_map(&prm.tm_v[1], vc, B, Nc, H, D))
     return ATTN_ERR_CUDA;
@@ -1113,7 +1132,7 @@ int run(const void* q, const void* kp, const void* vp, const void* kc, const voi
     prm.tm_v[0] = prm.tm_v[1];
   }
   const long long q_pairs = (static_cast<long long>(Nq) + 2 * ncp::BM - 1) / (2 * ncp::BM);
-  const long long n_units = static_cast<long long>(B) * H * q_pairs;
+  n_units = static_cast<long long>(B) * H * q_pairs;
   if (n_units > 0x7fffffffLL) return ATTN_ERR_SHAPE;
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.Nq = Nq;
@@ -1129,6 +1148,85 @@ int run(const void* q, const void* kp, const void* vp, const void* kc, const voi
     prm.fault_mode = g_fault_mode;
     prm.wait_limit_ns = g_wait_limit_ns;
   }
+  return ATTN_OK;
+}
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (in host code the array's name is only a host-side stand-in).
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[64] = {};
+
+int noalloc_scratch(int dev, void** addr) {
+  if (dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_addr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, ncp::g_noalloc_scratch) != cudaSuccess || !ptr) {
+      cudaGetLastError();
+      return ATTN_ERR_CUDA;
+    }
+    g_noalloc_addr[dev] = ptr;
+  }
+  *addr = g_noalloc_addr[dev];
+  return ATTN_OK;
+}
+
+// The schedule of launch<D> with the split workspace taken from the static
+// scratch: no allocation.  A schedule that would need more pieces than the
+// scratch holds is refused (ATTN_ERR_SHAPE); the counters are cleared on the
+// stream first, since an aborted earlier call may have left them non-zero.
+template <int D>
+int launch_noalloc(Params& prm, long long n_units, cudaStream_t stream) {
+  using C = ncp::Cfg<D>;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  static int sm_count[64] = {};
+  if (dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
+  if (sm_count[dev] == 0) {
+    int sms = 0;
+    if (cudaFuncSetAttribute(ncp::attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms < 1)
+      return ATTN_ERR_CUDA;
+    sm_count[dev] = sms;
+  }
+  const int sms = sm_count[dev];
+  const int T = prm.n_tiles[0] + prm.n_tiles[1];
+  const long long rem = n_units % sms;
+  long long pieces = 1;
+  if (rem > 0) {
+    pieces = sms / rem;
+    if (pieces > T / MIN_PIECE_TILES) pieces = T / MIN_PIECE_TILES;
+    if (pieces > MAX_PIECES) pieces = MAX_PIECES;
+  }
+  if (pieces < 2) pieces = 1;
+  const long long n_whole = pieces >= 2 ? n_units - rem : n_units;
+  const long long n_items = n_whole + (n_units - n_whole) * pieces;
+  if (n_items > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+  if ((n_units - n_whole) * pieces > ncp::NOALLOC_PIECES) return ATTN_ERR_SHAPE;
+  void* scratch = nullptr;
+  if (noalloc_scratch(dev, &scratch) != ATTN_OK) return ATTN_ERR_CUDA;
+  if (pieces >= 2 &&
+      cudaMemsetAsync(scratch, 0, ncp::NOALLOC_COUNT_BYTES, stream) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  prm.n_whole = static_cast<int>(n_whole);
+  prm.n_items = static_cast<int>(n_items);
+  prm.pieces = static_cast<int>(pieces);
+  prm.ws_count = static_cast<unsigned int*>(scratch);
+  prm.ws_part = reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) +
+                                         ncp::NOALLOC_COUNT_BYTES);
+  const int grid = n_items < sms ? static_cast<int>(n_items) : sms;
+  ncp::attn_fwd_kernel<D><<<grid, ncp::NUM_THREADS, C::SMEM_BYTES, stream>>>(prm);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int run(const void* q, const void* kp, const void* vp, const void* kc, const void* vc, void* out,
+        int B, int Nq, int Np, int Nc, int H, int D, cudaStream_t stream) {
+  Params prm;
+  long long n_units = 0;
+  const int rc = prepare(q, kp, vp, kc, vc, out, B, Nq, Np, Nc, H, D, prm, n_units);
+  if (rc != ATTN_OK) return rc;
   return D == 128 ? launch<128>(prm, n_units, stream) : launch<64>(prm, n_units, stream);
 }
 
@@ -1140,6 +1238,17 @@ int attn_dense_fwd(const void* q, const void* k, const void* v, void* out, int B
                    int D, cudaStream_t stream) {
   if (!k || !v) return ATTN_ERR_NULL;
   return run(q, nullptr, nullptr, k, v, out, B, N, 0, N, H, D, stream);
+}
+
+int attn_dense_fwd_noalloc(const void* q, const void* k, const void* v, void* out, int B, int N,
+                           int H, int D, cudaStream_t stream) {
+  if (!k || !v) return ATTN_ERR_NULL;
+  Params prm;
+  long long n_units = 0;
+  const int rc = prepare(q, nullptr, nullptr, k, v, out, B, N, 0, N, H, D, prm, n_units);
+  if (rc != ATTN_OK) return rc;
+  return D == 128 ? launch_noalloc<128>(prm, n_units, stream)
+                  : launch_noalloc<64>(prm, n_units, stream);
 }
 
 int attn_prefix_fwd(const void* q, const void* kp, const void* vp, const void* kc, const void* vc,
