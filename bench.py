@@ -204,6 +204,10 @@ def make_call(ncp, w, dev_in, out):
     if w.kind == "dense":
         q, k, v = dev_in
         return lambda stream=None: ncp.attn_dense_fwd(q, k, v, out, stream)
+    if w.kind == "block_causal":
+        q, k, v = dev_in
+        ids = workloads.image_ids(w).to(q.device)
+        return lambda stream=None: ncp.attn_block_causal_fwd(q, k, v, ids, out, stream)
     q, kp, vp, kc, vc = dev_in
     return lambda stream=None: ncp.attn_prefix_fwd(q, kp, vp, kc, vc, out, stream)
 
@@ -286,9 +290,15 @@ def cpu_oracle_sample(w, inputs_cpu, target_s: float):
     cores = len(os.sched_getaffinity(0))
     oracle.set_threads(cores)
     bits = [workloads.bf16_bits(t) for t in inputs_cpu]
-    fn = oracle.dense_attention_rows if w.kind == "dense" else oracle.prefix_attention_rows
+    if w.kind == "dense":
+        fn = oracle.dense_attention_rows
+    elif w.kind == "prefix":
+        fn = oracle.prefix_attention_rows
+    else:
+        ids = workloads.image_ids(w).numpy()
+        fn = lambda *a: oracle.block_causal_attention_rows(*a[:-1], ids, a[-1])  # noqa: E731
     total_rows = w.B * w.Nq * w.H
-    flops_per_row = 4 * w.n_keys * w.D
+    flops_per_row = 4 * w.visible_pairs * w.D / w.Nq  # mean over rows
     rng = np.random.default_rng(0)
     n = min(total_rows, 256)
     t0 = time.perf_counter()

@@ -77,6 +77,26 @@ int attn_prefix_fwd(const void *q, const void *kp, const void *vp, const void *k
                     cudaStream_t stream);
 
 /*
+ * Block-causal self-attention with image segments: the definition
+ * definitions/block_causal_attention/prefix_cached_block_causal_h32_d128_
+ * prefix0.json, field "reference" (the empty-prefix specialisation of the
+ * prefix-cached form).  Query i sees key j iff j <= i (text and different
+ * images are causal), or image_ids[i] == image_ids[j] >= 0 (tokens of one
+ * image see each other).  Scale D^-0.5.
+ *   q, k, v:   [B, N, H, D] bf16, device, read only.
+ *   image_ids: [N] int32, device, read only, shared by the batch; -1 marks a
+ *              text token, non-negative values name images.  Any ids give the
+ *              exact definition; ids that form contiguous, distinct image
+ *              blocks (the definition's engine segment list) let whole key
+ *              tiles be skipped.  Must be 16-byte aligned.
+ *   out:       [B, N, H, D] bf16, device, written; must not overlap an input.
+ * N <= 131072 (the per-CTA tile table lives in shared memory).  Returns
+ * ATTN_OK or a negative attn_status (ATTN_ERR_SHAPE for N too large).
+ */
+int attn_block_causal_fwd(const void *q, const void *k, const void *v, const int *image_ids,
+                          void *out, int B, int N, int H, int D, cudaStream_t stream);
+
+/*
  * attn_dense_fwd without any allocation, for callers that cannot call
  * cudaMalloc: an engine whose memory pool already owns the device memory, a
  * plugin that is handed only its input and output buffers, or a latency-bound

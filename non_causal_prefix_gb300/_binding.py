@@ -31,6 +31,7 @@ SIGNATURES = {
     "attn_debug_set_fault": (_I, [_I, ctypes.c_uint]),
     "attn_debug_exp2": (_I, [_VP, _VP, ctypes.c_longlong, _I, _VP]),
     "attn_dense_fwd_noalloc": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
+    "attn_block_causal_fwd": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
 }
 
 _lock = threading.Lock()
@@ -138,6 +139,33 @@ def attn_prefix_fwd(q, kp, vp, kc, vc, out, stream=None) -> None:
         kc.data_ptr(), vc.data_ptr(), out.data_ptr(), B, Nq, Np, Nc, H, D,
         _stream_handle(stream))
     _check(rc, "attn_prefix_fwd")
+
+
+def attn_block_causal_fwd(q, k, v, image_ids, out, stream=None) -> None:
+    """Enqueue block-causal attention: q, k, v, out CUDA bf16 [B, N, H, D];
+    image_ids a CUDA int32 tensor [N] (-1 = text token, >= 0 = image id)."""
+    import torch
+    B, N, H, D = _bnhd(q, "q")
+    for t, n in ((k, "k"), (v, "v"), (out, "out")):
+        if tuple(t.shape) != (B, N, H, D):
+            raise ValueError(f"{n} must have q's shape {tuple(q.shape)}")
+    if image_ids.dtype != torch.int32 or not image_ids.is_cuda or not image_ids.is_contiguous():
+        raise ValueError("image_ids must be a contiguous CUDA int32 tensor")
+    if tuple(image_ids.shape) != (N,):
+        raise ValueError("image_ids must be [N]")
+    _check_tensors(q, k, v, out)
+    rc = load_library().attn_block_causal_fwd(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), image_ids.data_ptr(), out.data_ptr(),
+        B, N, H, D, _stream_handle(stream))
+    _check(rc, "attn_block_causal_fwd")
+
+
+def block_causal_attention(q, k, v, image_ids, stream=None):
+    """Allocate ``out`` with torch and run ``attn_block_causal_fwd``."""
+    import torch
+    out = torch.empty_like(q)
+    attn_block_causal_fwd(q, k, v, image_ids, out, stream)
+    return out
 
 
 def _check_tensors(*ts):

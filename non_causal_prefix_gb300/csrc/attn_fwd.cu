@@ -44,6 +44,9 @@ constexpr uint32_t TMEM_COLS = 512;
 __host__ __device__ constexpr uint32_t tmem_s_col(int i) { return 128u * i; }
 __host__ __device__ constexpr uint32_t tmem_o_col(int i) { return 256u + 128u * i; }
 constexpr int MAX_SLOTS = 8;
+// Block-causal form: per-CTA table of the image ids in each 128-token tile
+// (min, max and "one image only"), held in shared memory; N <= 128 * this.
+constexpr int MAX_SEQ_TILES = 1024;
 // Rescale O only when the running row maximum (log2 units) grows by more than
 // this; otherwise keep the stale maximum.  Exact, because the final 1/l uses
 // the same maximum as the accumulated O, and p <= 2^8 stays far from overflow.
@@ -73,6 +76,8 @@ struct Cfg {
   static constexpr uint32_t Q_OFF = RING_OFF + NSLOT * TILE_BYTES;
   static constexpr uint32_t BAR_OFF = Q_OFF + 2 * TILE_BYTES;
   static constexpr uint32_t SMEM_BYTES = BAR_OFF + 512 + 1024;  // barriers + 1 KiB alignment slack
+  static constexpr uint32_t SUM_OFF = BAR_OFF + 512;             // block-causal tile table
+  static constexpr uint32_t SMEM_BYTES_BC = SUM_OFF + 3 * 4 * MAX_SEQ_TILES + 1024;
   // Share of the exponentials computed by the FMA-pipe polynomial instead of
   // the MUFU unit: POLY_NUM of every POLY_DEN packed pairs.  The MUFU unit does
   // 16 exp2 per clock per SM, as many as the S and P V MMAs need at D = 128;
@@ -105,6 +110,7 @@ struct Params {
   CUtensorMap tm_k[2];   // [0] prefix segment, [1] current segment
   CUtensorMap tm_v[2];
   __nv_bfloat16* out;
+  const int* image_ids;  // block-causal form: [Nq] image id per token, -1 = text
   int Nq, H;
   int q_pairs;           // ceil(Nq / 256): units per (b, h); units are (b, h, q pair), q pair fastest
   // Work items, walked round-robin by the persistent CTAs: items [0, n_whole)
@@ -409,9 +415,12 @@ struct Unit {
   bool two;  // the second 128-row query tile has at least one row
 };
 
+template <bool BC>
 __device__ __forceinline__ Unit decode_unit(const Params& p, int unit) {
   Unit u;
-  const int qp = unit % p.q_pairs;
+  // Block-causal rows see more keys the later they sit: hand out the last
+  // query pairs first (longest work first).
+  const int qp = BC ? p.q_pairs - 1 - unit % p.q_pairs : unit % p.q_pairs;
   const int bh = unit / p.q_pairs;
   u.h = bh % p.H;
   u.b = bh / p.H;
@@ -427,6 +436,7 @@ struct Item {
   int piece;
 };
 
+template <bool BC>
 __device__ __forceinline__ Item decode_item(const Params& p, int item, int T) {
   Item it;
   int unit;
@@ -445,16 +455,55 @@ __device__ __forceinline__ Item decode_item(const Params& p, int item, int T) {
     it.t_begin = (k * T) / p.pieces;
     it.t_end = ((k + 1) * T) / p.pieces;
   }
-  it.u = decode_unit(p, unit);
+  it.u = decode_unit<BC>(p, unit);
   return it;
 }
+
+// Block-causal visibility (definition prefix_cached_block_causal_h32_d128_
+// prefix0): query i sees key j iff j <= i, or both carry the same image id >= 0.
+// Tiles are summarised by the range [lo, hi] of their non-negative ids (lo >
+// hi: text only) and by `uni` (every token in one image).
+struct TileTable {
+  const int* lo;
+  const int* hi;
+  const int* uni;
+};
+
+// Some query row of the unit sees some key of tile t: causally (the tile
+// starts at or before the unit's last row), or through an image id both may
+// share (their id ranges meet).  Exact as a filter: a skipped tile has no
+// visible pair.
+__device__ __forceinline__ bool bc_unit_visits(const TileTable& tt, const Unit& u, int N, int t) {
+  const int r_last = min(u.q0 + 2 * BM, N) - 1;
+  if (t * BN <= r_last) return true;
+  const int qt0 = u.q0 / BM;
+  const int qt1 = u.two ? qt0 + 1 : qt0;
+  const int qlo = min(tt.lo[qt0], tt.lo[qt1]);
+  const int qhi = max(tt.hi[qt0], tt.hi[qt1]);
+  return qlo <= tt.hi[t] && tt.lo[t] <= qhi;
+}
+
+// Every query row of query tile qt (first row q_first) sees every key of tile
+// t: the keys all precede the rows, or both tiles hold one and the same image.
+__device__ __forceinline__ bool bc_tile_full(const TileTable& tt, int qt, int q_first, int t) {
+  if (t * BN + BN - 1 <= q_first) return true;
+  return tt.uni[qt] && tt.uni[t] && tt.lo[qt] == tt.lo[t];
+}
+
+// Per-row mask of one key tile of the block-causal form: key c0 + c is visible
+// to query row qi (image id idq) iff c0 + c <= qi or its id equals idq >= 0.
+struct RowMask {
+  const int* ids;  // image ids of the tile's keys (ids[0] is key c0); nullptr: all visible
+  int c0, qi, idq, n;  // n: keys of the sequence (ids past n are not read)
+};
 
 // One 128-key tile of the online softmax for this thread's query row:
 // S (fp32, TMEM) -> running max m and sum l (log2 domain) -> P (bf16) written
 // over the first 64 columns of S; O is rescaled in TMEM when m moved.
-template <int D>
+template <int D, bool BC>
 __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, int valid, float sl2,
-                                             bool may_rescale, float& m, float& l) {
+                                             bool may_rescale, const RowMask& mask, float& m,
+                                             float& l) {
   float s[BN];
   {
     uint32_t r[BN];
@@ -468,6 +517,28 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, i
 #pragma unroll
     for (int c = 0; c < BN; ++c)
       if (c >= valid) s[c] = -INFINITY;
+  }
+  if (BC && mask.ids) {
+    const int lim = mask.qi - mask.c0;  // keys c <= lim are visible causally
+    if (mask.c0 + BN <= mask.n) {
+      const int4* ids4 = reinterpret_cast<const int4*>(mask.ids);
+#pragma unroll
+      for (int c = 0; c < BN; c += 4) {
+        const int4 id = __ldg(ids4 + c / 4);
+        const bool img = mask.idq >= 0;
+        if (!(c + 0 <= lim || (img && id.x == mask.idq))) s[c + 0] = -INFINITY;
+        if (!(c + 1 <= lim || (img && id.y == mask.idq))) s[c + 1] = -INFINITY;
+        if (!(c + 2 <= lim || (img && id.z == mask.idq))) s[c + 2] = -INFINITY;
+        if (!(c + 3 <= lim || (img && id.w == mask.idq))) s[c + 3] = -INFINITY;
+      }
+    } else {
+      // Last tile of the sequence: keys past n are already masked (valid).
+#pragma unroll
+      for (int c = 0; c < BN; ++c) {
+        const int id = (mask.c0 + c < mask.n) ? __ldg(mask.ids + c) : -1;
+        if (!(c <= lim || (mask.idq >= 0 && id == mask.idq))) s[c] = -INFINITY;
+      }
+    }
   }
   // Row maximum: four independent chains of 3-input max.
   float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
@@ -493,7 +564,10 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, i
   // p = 2^(s * scale * log2(e) - m) on packed pairs; pairs selected by
   // poly_pair go through the FMA-pipe polynomial, the rest through MUFU.
   const uint64_t sl2x2 = pk2(sl2, sl2);
-  const uint64_t neg_m2 = pk2(-m, -m);
+  // A row with no visible key yet (block-causal form only) keeps m = -inf:
+  // use 0 so that its masked scores give p = 0 instead of NaN.
+  const float m_ref = (BC && m == -INFINITY) ? 0.f : m;
+  const uint64_t neg_m2 = pk2(-m_ref, -m_ref);
   uint64_t acc0 = 0, acc1 = 0;  // two packed running sums (bits 0 = 0.0f)
   uint32_t pk[BN / 2];
 #pragma unroll
@@ -547,7 +621,9 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, i
 // ----------------------------------------------------------------------------
 // The kernel
 // ----------------------------------------------------------------------------
-template <int D>
+// BC = false: dense and prefix-cached forms (every key visible).
+// BC = true: block-causal form (one key segment, per-row image-id mask).
+template <int D, bool BC>
 // 10 warps on 4 SM sub-partitions (16 Ki registers each, 3 warps on two of
 // them) cap a thread at 168 registers.
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -607,6 +683,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  // Block-causal form: summarise the image ids of every 128-token tile.
+  const int n_seq = p.Nq;
+  TileTable tt{nullptr, nullptr, nullptr};
+  if constexpr (BC) {
+    int* t_lo = reinterpret_cast<int*>(base + C::SUM_OFF);
+    int* t_hi = t_lo + MAX_SEQ_TILES;
+    int* t_uni = t_hi + MAX_SEQ_TILES;
+    for (int t = warp; t < p.n_tiles[1]; t += NUM_THREADS / 32) {
+      int lo = 0x7fffffff, hi = -1;
+      bool text = false;
+      for (int e = lane; e < BN; e += 32) {
+        const int j = t * BN + e;
+        if (j < n_seq) {
+          const int id = __ldg(p.image_ids + j);
+          if (id < 0) {
+            text = true;
+          } else {
+            lo = min(lo, id);
+            hi = max(hi, id);
+          }
+        }
+      }
+      lo = __reduce_min_sync(0xffffffffu, lo);
+      hi = __reduce_max_sync(0xffffffffu, hi);
+      text = __any_sync(0xffffffffu, text);
+      if (lane == 0) {
+        t_lo[t] = lo;
+        t_hi[t] = hi;
+        t_uni[t] = (!text && lo == hi) ? 1 : 0;
+      }
+    }
+    tt = TileTable{t_lo, t_hi, t_uni};
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -628,7 +737,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int n = 0;  // units done by this CTA
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += stride, ++n) {
-        const Item it = decode_item(p, item, T);
+        const Item it = decode_item<BC>(p, item, T);
         const Unit& u = it.u;
         // The Q buffers are free once every S MMA of the previous item is done.
         if (n > 0) {
@@ -643,6 +752,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         u.q0 + i * BM, u.b, bar_q);
         q_last = n;
         for (int t = it.t_begin; t < it.t_end && ok; ++t) {
+          if (BC && !bc_unit_visits(tt, u, n_seq, t)) continue;
           const int seg = (t < T0) ? 0 : 1;
           const int tok0 = (t - (seg ? T0 : 0)) * BN;
           for (int kind = 0; kind < 2; ++kind) {
@@ -711,13 +821,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         return true;
       };
       for (int item = blockIdx.x; item < n_items && ok; item += stride, ++n) {
-        const Item it = decode_item(p, item, T);
+        const Item it = decode_item<BC>(p, item, T);
         const int nq = it.u.two ? 2 : 1;
-        const int nt = it.t_end - it.t_begin;
         ok = wait_bounded(bar_q, n & 1, limit, abort_flag, 2);
         if (!ok) break;
         int v_prev = -1;
-        for (int j = 0; j < nt && ok; ++j) {
+        int j = 0;  // key tiles visited so far in this item
+        for (int t = it.t_begin; t < it.t_end && ok; ++t) {
+          if (BC && !bc_unit_visits(tt, it.u, n_seq, t)) continue;
           const int k_slot = slot;
           ok = wait_bounded(bar_kv_full(k_slot), phase, limit, abort_flag, 3);
           if (!ok) break;
@@ -740,11 +851,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!ok) break;
           if (++slot == C::NSLOT) { slot = 0; phase ^= 1u; }
           v_prev = v_slot;
+          ++j;
         }
         if (!ok) break;
         mma_commit(bar_qfree);  // every S MMA of this item has been issued
         for (int i = 0; i < nq && ok; ++i) {
-          ok = pv(i, v_prev, nt - 1 > 0);
+          ok = pv(i, v_prev, j - 1 > 0);
           if (!ok) break;
           mma_commit(bar_o[i]);
           ++oc[i];
@@ -768,12 +880,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t bar_merge = smem_u32(&ctl->merge_ready[i]);
     const int row = wq * 32 + lane;  // row of the 128-row query tile (= TMEM lane)
     for (int item = blockIdx.x; item < n_items && ok; item += stride) {
-      const Item it = decode_item(p, item, T);
+      const Item it = decode_item<BC>(p, item, T);
       const Unit& u = it.u;
       if (i == 1 && !u.two) continue;
       float m = -INFINITY;  // running (possibly stale) maximum, log2 units
       float l = 0.f;        // running sum of exp2(x - m)
+      RowMask mask{nullptr, 0, 0, -1, n_seq};
+      if constexpr (BC) {
+        mask.qi = u.q0 + i * BM + row;
+        mask.idq = mask.qi < n_seq ? __ldg(p.image_ids + mask.qi) : -1;
+      }
+      int j = 0;  // key tiles visited so far in this item
       for (int t = it.t_begin; t < it.t_end; ++t) {
+        if constexpr (BC) {
+          if (!bc_unit_visits(tt, u, n_seq, t)) continue;
+          const bool full = bc_tile_full(tt, u.q0 / BM + i, u.q0 + i * BM, t);
+          mask.ids = full ? nullptr : p.image_ids + t * BN;
+          mask.c0 = t * BN;
+        }
         ok = warp_wait(bar_s[i], sc & 1u, limit, abort_flag, 7);
         if (!ok) break;
         ++sc;
@@ -782,7 +906,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // scores must be -inf instead.
         const int seg = (t < T0) ? 0 : 1;
         const int valid = p.n_tok[seg] - (t - (seg ? T0 : 0)) * BN;
-        softmax_tile<D>(s_addr, o_addr, valid, sl2, t > it.t_begin, m, l);
+        softmax_tile<D, BC>(s_addr, o_addr, valid, sl2, j > 0, mask, m, l);
+        ++j;
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
@@ -1056,17 +1181,18 @@ const Workspace* get_workspace(int dev, int sms, cudaStream_t stream) {
   return &(g_ws[key] = ws);
 }
 
-template <int D>
+template <int D, bool BC>
 int launch(Params& prm, long long n_units, cudaStream_t stream) {
   using C = ncp::Cfg<D>;
+  constexpr uint32_t smem = BC ? C::SMEM_BYTES_BC : C::SMEM_BYTES;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
   static int sm_count[64] = {};  // per device, 0 = not configured yet
   if (dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
   if (sm_count[dev] == 0) {
     int sms = 0;
-    if (cudaFuncSetAttribute(ncp::attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_BYTES) != cudaSuccess ||
+    if (cudaFuncSetAttribute(ncp::attn_fwd_kernel<D, BC>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         sms < 1)
       return ATTN_ERR_CUDA;
@@ -1079,7 +1205,9 @@ int launch(Params& prm, long long n_units, cudaStream_t stream) {
   const int T = prm.n_tiles[0] + prm.n_tiles[1];
   const long long rem = n_units % sms;
   long long pieces = 1;
-  if (rem > 0) {
+  // The block-causal form visits a data-dependent subset of the key tiles, so
+  // a fixed key range could hold none of them: its units are never split.
+  if (rem > 0 && !BC) {
     pieces = sms / rem;
     if (pieces > T / MIN_PIECE_TILES) pieces = T / MIN_PIECE_TILES;
     if (pieces > MAX_PIECES) pieces = MAX_PIECES;
@@ -1097,14 +1225,14 @@ int launch(Params& prm, long long n_units, cudaStream_t stream) {
   // Persistent grid: one CTA per SM (shared memory and TMEM allow one), each
   // walking the items round-robin.
   const int grid = n_items < sms ? static_cast<int>(n_items) : sms;
-  ncp::attn_fwd_kernel<D><<<grid, ncp::NUM_THREADS, C::SMEM_BYTES, stream>>>(prm);
+  ncp::attn_fwd_kernel<D, BC><<<grid, ncp::NUM_THREADS, smem, stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 // Argument checks, TMA descriptors and kernel parameters of one call.
 int prepare(const void* q, const void* kp, const void* vp, const void* kc, const void* vc,
-            void* out, int B, int Nq, int Np, int Nc, int H, int D, Params& prm,
-            long long& n_units) {
+            const int* image_ids, void* out, int B, int Nq, int Np, int Nc, int H, int D,
+            Params& prm, long long& n_units) {
   if (!q || !kc || !vc || !out || (Np > 0 && (!kp || !vp))) return ATTN_ERR_NULL;
   if (B < 1 || Nq < 1 || Nc < 1 || H < 1 || Np < 0) return ATTN_ERR_SHAPE;
   if (H > 65535 || B > 65535) return ATTN_ERR_SHAPE;
@@ -1135,6 +1263,7 @@ int prepare(const void* q, const void* kp, const void* vp, const void* kc, const
   n_units = static_cast<long long>(B) * H * q_pairs;
   if (n_units > 0x7fffffffLL) return ATTN_ERR_SHAPE;
   prm.out = static_cast<__nv_bfloat16*>(out);
+  prm.image_ids = image_ids;
   prm.Nq = Nq;
   prm.H = H;
   prm.q_pairs = static_cast<int>(q_pairs);
@@ -1184,8 +1313,8 @@ int launch_noalloc(Params& prm, long long n_units, cudaStream_t stream) {
   if (dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
   if (sm_count[dev] == 0) {
     int sms = 0;
-    if (cudaFuncSetAttribute(ncp::attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_BYTES) != cudaSuccess ||
+    if (cudaFuncSetAttribute(ncp::attn_fwd_kernel<D, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         sms < 1)
       return ATTN_ERR_CUDA;
@@ -1217,17 +1346,22 @@ int launch_noalloc(Params& prm, long long n_units, cudaStream_t stream) {
   prm.ws_part = reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) +
                                          ncp::NOALLOC_COUNT_BYTES);
   const int grid = n_items < sms ? static_cast<int>(n_items) : sms;
-  ncp::attn_fwd_kernel<D><<<grid, ncp::NUM_THREADS, C::SMEM_BYTES, stream>>>(prm);
+  ncp::attn_fwd_kernel<D, false><<<grid, ncp::NUM_THREADS, C::SMEM_BYTES, stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int run(const void* q, const void* kp, const void* vp, const void* kc, const void* vc, void* out,
-        int B, int Nq, int Np, int Nc, int H, int D, cudaStream_t stream) {
+int run(const void* q, const void* kp, const void* vp, const void* kc, const void* vc,
+        const int* image_ids, void* out, int B, int Nq, int Np, int Nc, int H, int D,
+        cudaStream_t stream) {
   Params prm;
   long long n_units = 0;
-  const int rc = prepare(q, kp, vp, kc, vc, out, B, Nq, Np, Nc, H, D, prm, n_units);
+  const int rc = prepare(q, kp, vp, kc, vc, image_ids, out, B, Nq, Np, Nc, H, D, prm, n_units);
   if (rc != ATTN_OK) return rc;
-  return D == 128 ? launch<128>(prm, n_units, stream) : launch<64>(prm, n_units, stream);
+  if (image_ids)
+    return D == 128 ? launch<128, true>(prm, n_units, stream)
+                    : launch<64, true>(prm, n_units, stream);
+  return D == 128 ? launch<128, false>(prm, n_units, stream)
+                  : launch<64, false>(prm, n_units, stream);
 }
 
 }  // namespace
@@ -1237,7 +1371,19 @@ extern "C" {
 int attn_dense_fwd(const void* q, const void* k, const void* v, void* out, int B, int N, int H,
                    int D, cudaStream_t stream) {
   if (!k || !v) return ATTN_ERR_NULL;
-  return run(q, nullptr, nullptr, k, v, out, B, N, 0, N, H, D, stream);
+  return run(q, nullptr, nullptr, k, v, nullptr, out, B, N, 0, N, H, D, stream);
+}
+
+int attn_block_causal_fwd(const void* q, const void* k, const void* v, const int* image_ids,
+                          void* out, int B, int N, int H, int D, cudaStream_t stream) {
+  if (!k || !v || !image_ids) return ATTN_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(image_ids) & 15u) != 0) return ATTN_ERR_ALIGN;
+  if (N > ncp::MAX_SEQ_TILES * ncp::BN) return ATTN_ERR_SHAPE;
+  if (B >= 1 && N >= 1 && H >= 1 && D >= 1 &&
+      overlaps(out, static_cast<size_t>(B) * N * H * D * 2, image_ids,
+               static_cast<size_t>(N) * sizeof(int)))
+    return ATTN_ERR_ALIAS;
+  return run(q, nullptr, nullptr, k, v, image_ids, out, B, N, 0, N, H, D, stream);
 }
 
 int attn_dense_fwd_noalloc(const void* q, const void* k, const void* v, void* out, int B, int N,
@@ -1245,7 +1391,7 @@ int attn_dense_fwd_noalloc(const void* q, const void* k, const void* v, void* ou
   if (!k || !v) return ATTN_ERR_NULL;
   Params prm;
   long long n_units = 0;
-  const int rc = prepare(q, nullptr, nullptr, k, v, out, B, N, 0, N, H, D, prm, n_units);
+  const int rc = prepare(q, nullptr, nullptr, k, v, nullptr, out, B, N, 0, N, H, D, prm, n_units);
   if (rc != ATTN_OK) return rc;
   return D == 128 ? launch_noalloc<128>(prm, n_units, stream)
                   : launch_noalloc<64>(prm, n_units, stream);
@@ -1253,7 +1399,7 @@ int attn_dense_fwd_noalloc(const void* q, const void* k, const void* v, void* ou
 
 int attn_prefix_fwd(const void* q, const void* kp, const void* vp, const void* kc, const void* vc,
                     void* out, int B, int Nq, int Np, int Nc, int H, int D, cudaStream_t stream) {
-  return run(q, kp, vp, kc, vc, out, B, Nq, Np, Nc, H, D, stream);
+  return run(q, kp, vp, kc, vc, nullptr, out, B, Nq, Np, Nc, H, D, stream);
 }
 
 const char* attn_status_string(int status) {

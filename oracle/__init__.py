@@ -4,12 +4,14 @@ Only the tests, ``__graft_entry__.smoke()`` and the bench's CPU-baseline leg
 import this package.  The product path (``non_causal_prefix_gb300``) never
 does, and this package never imports the product path.
 
-The arithmetic lives in ``attn_oracle.c`` (plain C, FP64, OpenMP over output
-rows); this module only compiles it with gcc and marshals numpy arrays.
+The arithmetic lives in ``attn_oracle.c`` (dense and prefix-cached forms) and
+``attn_oracle_block_causal.c`` (plain C, FP64, OpenMP over output rows); this
+module only compiles them with gcc into one library and marshals numpy arrays.
 Inputs are bf16 bit patterns (``numpy.uint16``, layout ``[B, N, H, D]``);
 outputs are float64 ``[B, Nq, H, D]`` (or ``[rows, D]`` for sampled rows).
 
-Pins: every function here is checked in ``tests/test_oracle.py`` against
+Pins: the dense and prefix functions are checked in ``tests/test_oracle.py``,
+the block-causal ones in ``tests/test_oracle_block_causal.py``, against
 closed forms (one key; identical keys; one dominant logit; the two-key
 logistic weight), invariants (joint K/V permutation, query/head/batch
 independence, prefix == dense on the explicit concatenation), a pure-Python
@@ -26,6 +28,8 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 SOURCE = os.path.join(_HERE, "attn_oracle.c")
+SOURCE_BLOCK_CAUSAL = os.path.join(_HERE, "attn_oracle_block_causal.c")
+SOURCES = [SOURCE, SOURCE_BLOCK_CAUSAL]
 _LIB_DIR = os.path.join(_HERE, "_lib")
 _LIB = os.path.join(_LIB_DIR, "liboracle.so")
 _lock = threading.Lock()
@@ -35,10 +39,11 @@ GCC_FLAGS = ["-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-fno-fast-math"
              "-ffp-contract=off"]
 
 
-def compile_source(src: str, out: str) -> str:
-    """Compile one C source of the oracle into a shared library at ``out``."""
+def compile_source(src, out: str) -> str:
+    """Compile C source(s) of the oracle (a path or a list) into a shared library at ``out``."""
+    srcs = [src] if isinstance(src, str) else list(src)
     tmp = out + f".tmp{os.getpid()}"
-    subprocess.run(["gcc", *GCC_FLAGS, "-o", tmp, src, "-lm"], check=True)
+    subprocess.run(["gcc", *GCC_FLAGS, "-o", tmp, *srcs, "-lm"], check=True)
     os.replace(tmp, out)
     return out
 
@@ -47,9 +52,9 @@ def build(force: bool = False) -> str:
     """Compile the oracle with gcc (-O2, OpenMP, no fast-math) if stale."""
     os.makedirs(_LIB_DIR, exist_ok=True)
     if (not force and os.path.exists(_LIB)
-            and os.path.getmtime(_LIB) >= os.path.getmtime(SOURCE)):
+            and all(os.path.getmtime(_LIB) >= os.path.getmtime(f) for f in SOURCES)):
         return _LIB
-    return compile_source(SOURCE, _LIB)
+    return compile_source(SOURCES, _LIB)
 
 
 def _u16(a: np.ndarray) -> np.ndarray:
@@ -88,6 +93,16 @@ class Oracle:
                   "oracle_prefix_attention", "oracle_prefix_attention_rows",
                   "oracle_max_threads"):
             getattr(lib, f).restype = ci
+        # The block-causal form lives in its own source; a library built from
+        # attn_oracle.c alone (the tests' single-file mutants) lacks it.
+        if hasattr(lib, "oracle_block_causal_attention"):
+            i32p = ctypes.POINTER(ctypes.c_int32)
+            lib.oracle_block_causal_attention.argtypes = [
+                u16p, u16p, u16p, i32p, f64p, ci, ci, ci, ci]
+            lib.oracle_block_causal_attention_rows.argtypes = [
+                u16p, u16p, u16p, i32p, f64p, ci, ci, ci, ci, i64p, ctypes.c_int64]
+            lib.oracle_block_causal_attention.restype = ci
+            lib.oracle_block_causal_attention_rows.restype = ci
         lib.oracle_set_threads.argtypes = [ci]
         lib.oracle_set_threads.restype = None
         self.lib = lib
@@ -170,6 +185,40 @@ class Oracle:
             _ptr(rows, ctypes.c_int64), rows.size), "oracle_prefix_attention_rows")
         return out
 
+    def block_causal_attention(self, Q, K, V, image_ids) -> np.ndarray:
+        """Block-causal self-attention in FP64: query i sees key j iff j <= i or
+        both carry the same image id >= 0.  Q/K/V [B,N,H,D], image_ids [N]."""
+        Q, K, V = _u16(Q), _u16(K), _u16(V)
+        B, N, H, D = Q.shape
+        if K.shape != Q.shape or V.shape != Q.shape:
+            raise ValueError("Q, K, V must all be [B, N, H, D]")
+        ids = np.ascontiguousarray(image_ids, dtype=np.int32)
+        if ids.shape != (N,):
+            raise ValueError("image_ids must be [N]")
+        out = np.empty((B, N, H, D), dtype=np.float64)
+        _check(self.lib.oracle_block_causal_attention(
+            _ptr(Q, ctypes.c_uint16), _ptr(K, ctypes.c_uint16), _ptr(V, ctypes.c_uint16),
+            _ptr(ids, ctypes.c_int32), _ptr(out, ctypes.c_double), B, N, H, D),
+            "oracle_block_causal_attention")
+        return out
+
+    def block_causal_attention_rows(self, Q, K, V, image_ids, rows) -> np.ndarray:
+        """Sampled rows of ``block_causal_attention`` (flat row r = (b*N + i)*H + h)."""
+        Q, K, V = _u16(Q), _u16(K), _u16(V)
+        B, N, H, D = Q.shape
+        if K.shape != Q.shape or V.shape != Q.shape:
+            raise ValueError("Q, K, V must all be [B, N, H, D]")
+        ids = np.ascontiguousarray(image_ids, dtype=np.int32)
+        if ids.shape != (N,):
+            raise ValueError("image_ids must be [N]")
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        out = np.empty((rows.size, D), dtype=np.float64)
+        _check(self.lib.oracle_block_causal_attention_rows(
+            _ptr(Q, ctypes.c_uint16), _ptr(K, ctypes.c_uint16), _ptr(V, ctypes.c_uint16),
+            _ptr(ids, ctypes.c_int32), _ptr(out, ctypes.c_double), B, N, H, D,
+            _ptr(rows, ctypes.c_int64), rows.size), "oracle_block_causal_attention_rows")
+        return out
+
 
 def default() -> Oracle:
     """The oracle compiled from ``attn_oracle.c`` (built on first use)."""
@@ -202,3 +251,11 @@ def prefix_attention(Q, K_prefix, V_prefix, K_current, V_current) -> np.ndarray:
 
 def prefix_attention_rows(Q, K_prefix, V_prefix, K_current, V_current, rows) -> np.ndarray:
     return default().prefix_attention_rows(Q, K_prefix, V_prefix, K_current, V_current, rows)
+
+
+def block_causal_attention(Q, K, V, image_ids) -> np.ndarray:
+    return default().block_causal_attention(Q, K, V, image_ids)
+
+
+def block_causal_attention_rows(Q, K, V, image_ids, rows) -> np.ndarray:
+    return default().block_causal_attention_rows(Q, K, V, image_ids, rows)

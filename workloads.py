@@ -38,6 +38,8 @@ class Workload:
     D: int
     sigma: float
     Np: int = 0      # prefix length (prefix form only)
+    # Block-causal form: the token sequence as (image id, length) runs; -1 = text.
+    segments: tuple = ()
 
     @property
     def n_keys(self) -> int:
@@ -45,9 +47,23 @@ class Workload:
         return self.Np + self.Nk
 
     @property
+    def visible_pairs(self) -> int:
+        """(query, key) pairs that enter the softmax, per (batch, head)."""
+        if self.kind != "block_causal":
+            return self.Nq * self.n_keys
+        total, pos = 0, 0
+        for ident, length in self.segments:
+            if ident < 0:          # text: token i sees keys 0..i
+                total += sum(pos + r + 1 for r in range(length))
+            else:                  # an image block [pos, pos+length): every token sees 0..end-1
+                total += length * (pos + length)
+            pos += length
+        return total
+
+    @property
     def flops(self) -> int:
-        """Algorithmic FLOPs: 2*D per score (QK^T) + 2*D per score (PV)."""
-        return 4 * self.B * self.H * self.Nq * self.n_keys * self.D
+        """Algorithmic FLOPs: 2*D per visible score (QK^T) + 2*D per visible score (PV)."""
+        return 4 * self.B * self.H * self.visible_pairs * self.D
 
     @property
     def hbm_bytes(self) -> int:
@@ -59,12 +75,16 @@ class Workload:
         """Shapes of the inputs, in operand order."""
         q = (self.B, self.Nq, self.H, self.D)
         kv = (self.B, self.Nk, self.H, self.D)
-        if self.kind == "dense":
+        if self.kind in ("dense", "block_causal"):
             return [q, kv, kv]
         p = (self.B, self.Np, self.H, self.D)
         return [q, p, p, kv, kv]
 
     def describe(self) -> str:
+        if self.kind == "block_causal":
+            runs = "+".join(f"{'text' if i < 0 else 'img' + str(i)}:{n}" for i, n in self.segments)
+            return (f"block-causal B={self.B} N={self.Nq} ({runs}) H={self.H} D={self.D} "
+                    f"sigma={self.sigma}")
         if self.kind == "dense":
             return (f"dense B={self.B} N={self.Nq} H={self.H} D={self.D} "
                     f"sigma={self.sigma}")
@@ -73,7 +93,11 @@ class Workload:
 
 
 # The five synthetic configurations.  1-3 and 5 are dense self-attention,
-# 4 is the prefix-cached form with a 1024-token prefix.
+# 4 is the prefix-cached form with a 1024-token prefix.  6 is the block-causal
+# (empty-prefix) form of the same model's first evaluation: a text prompt, a
+# condition image, a short text run and the target image, each image a
+# contiguous block with its own id (definition prefix_cached_block_causal_h32_
+# d128_prefix0: "image_ids still represents the engine segment list").
 WORKLOADS = {
     1: Workload(1, "dense_b1_n128_h32_d64", "dense", 1, 128, 128, 32, 64, 1.0),
     2: Workload(2, "dense_b1_n4096_h32_d128", "dense", 1, 4096, 4096, 32, 128, 1.0),
@@ -81,6 +105,8 @@ WORKLOADS = {
     4: Workload(4, "prefix_b1_nq4096_np1024_h32_d128", "prefix", 1, 4096, 4096, 32,
                 128, 1.0, Np=1024),
     5: Workload(5, "dense_b1_n32768_h32_d128", "dense", 1, 32768, 32768, 32, 128, 0.5),
+    6: Workload(6, "block_causal_b1_n4448_h32_d128", "block_causal", 1, 4448, 4448, 32, 128,
+                1.0, segments=((-1, 333), (0, 2048), (-1, 19), (1, 2048))),
 }
 
 
@@ -100,10 +126,18 @@ def make_inputs(w: Workload, seed_base: int | None = None):
 
 
 def custom(kind: str, B: int, Nq: int, Nk: int, H: int, D: int, sigma: float = 1.0,
-           Np: int = 0, config_id: int = 0) -> Workload:
+           Np: int = 0, config_id: int = 0, segments: tuple = ()) -> Workload:
     """A workload of arbitrary shape (used for small parity and edge cases)."""
     name = f"{kind}_b{B}_nq{Nq}_nk{Nk}_np{Np}_h{H}_d{D}"
-    return Workload(config_id, name, kind, B, Nq, Nk, H, D, sigma, Np=Np)
+    if segments:
+        assert sum(n for _, n in segments) == Nq == Nk
+    return Workload(config_id, name, kind, B, Nq, Nk, H, D, sigma, Np=Np, segments=segments)
+
+
+def image_ids(w: Workload) -> torch.Tensor:
+    """The [N] int32 image-id vector of a block-causal workload (CPU)."""
+    parts = [torch.full((n,), ident, dtype=torch.int32) for ident, n in w.segments]
+    return torch.cat(parts) if parts else torch.empty(0, dtype=torch.int32)
 
 
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
