@@ -204,6 +204,9 @@ def make_call(ncp, w, dev_in, out):
     if w.kind == "dense":
         q, k, v = dev_in
         return lambda stream=None: ncp.attn_dense_fwd(q, k, v, out, stream)
+    if w.kind == "cross":
+        q, k, v = dev_in
+        return lambda stream=None: ncp.attn_dense_cross_fwd(q, k, v, out, stream)
     if w.kind == "block_causal":
         q, k, v = dev_in
         ids = workloads.image_ids(w).to(q.device)
@@ -290,7 +293,7 @@ def cpu_oracle_sample(w, inputs_cpu, target_s: float):
     cores = len(os.sched_getaffinity(0))
     oracle.set_threads(cores)
     bits = [workloads.bf16_bits(t) for t in inputs_cpu]
-    if w.kind == "dense":
+    if w.kind in ("dense", "cross"):
         fn = oracle.dense_attention_rows
     elif w.kind == "prefix":
         fn = oracle.prefix_attention_rows

@@ -63,6 +63,21 @@ int attn_dense_fwd(const void *q, const void *k, const void *v, void *out,
                    int B, int N, int H, int D, cudaStream_t stream);
 
 /*
+ * Dense non-causal cross attention: the same definitions as attn_dense_fwd,
+ * whose description allows it ("self attention uses Nq=Nk; cross attention
+ * allows unequal lengths").
+ *   q:    [B, Nq, H, D] bf16, device, read only.
+ *   k, v: [B, Nk, H, D] bf16, device, read only.
+ *   out:  [B, Nq, H, D] bf16, device, written.
+ * Nq, Nk >= 1.  When the (b, h, 256-query) work units are fewer than the
+ * SMs, each unit's keys are cut into pieces on separate SMs and merged (the
+ * split workspace, see attn_prefix_fwd), so short-query, long-context calls
+ * still fill the GPU.  Returns ATTN_OK or a negative attn_status.
+ */
+int attn_dense_cross_fwd(const void *q, const void *k, const void *v, void *out,
+                         int B, int Nq, int Nk, int H, int D, cudaStream_t stream);
+
+/*
  * Prefix-cached full-visibility attention.
  *   q:      [B, Nq, H, D]
  *   kp, vp: [B, Np, H, D]  cached prefix keys/values (may be NULL when Np == 0)

@@ -32,6 +32,7 @@ SIGNATURES = {
     "attn_debug_exp2": (_I, [_VP, _VP, ctypes.c_longlong, _I, _VP]),
     "attn_dense_fwd_noalloc": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
     "attn_block_causal_fwd": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
+    "attn_dense_cross_fwd": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
 }
 
 _lock = threading.Lock()
@@ -116,6 +117,21 @@ def attn_dense_fwd_noalloc(q, k, v, out, stream=None) -> None:
     rc = load_library().attn_dense_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(),
                                                out.data_ptr(), B, N, H, D, _stream_handle(stream))
     _check(rc, "attn_dense_fwd_noalloc")
+
+
+def attn_dense_cross_fwd(q, k, v, out, stream=None) -> None:
+    """Enqueue dense cross attention: q, out [B, Nq, H, D]; k, v [B, Nk, H, D]."""
+    B, Nq, H, D = _bnhd(q, "q")
+    Bk, Nk, Hk, Dk = _bnhd(k, "k")
+    if (Bk, Hk, Dk) != (B, H, D) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k/v must be [B, Nk, H, D] with q's B, H, D")
+    if tuple(out.shape) != (B, Nq, H, D):
+        raise ValueError("out must have q's shape")
+    _check_tensors(q, k, v, out)
+    rc = load_library().attn_dense_cross_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                             out.data_ptr(), B, Nq, Nk, H, D,
+                                             _stream_handle(stream))
+    _check(rc, "attn_dense_cross_fwd")
 
 
 def attn_prefix_fwd(q, kp, vp, kc, vc, out, stream=None) -> None:

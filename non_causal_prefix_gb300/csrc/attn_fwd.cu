@@ -1374,6 +1374,12 @@ int attn_dense_fwd(const void* q, const void* k, const void* v, void* out, int B
   return run(q, nullptr, nullptr, k, v, nullptr, out, B, N, 0, N, H, D, stream);
 }
 
+int attn_dense_cross_fwd(const void* q, const void* k, const void* v, void* out, int B, int Nq,
+                         int Nk, int H, int D, cudaStream_t stream) {
+  if (!k || !v) return ATTN_ERR_NULL;
+  return run(q, nullptr, nullptr, k, v, nullptr, out, B, Nq, 0, Nk, H, D, stream);
+}
+
 int attn_block_causal_fwd(const void* q, const void* k, const void* v, const int* image_ids,
                           void* out, int B, int N, int H, int D, cudaStream_t stream) {
   if (!k || !v || !image_ids) return ATTN_ERR_NULL;

@@ -75,7 +75,7 @@ class Workload:
         """Shapes of the inputs, in operand order."""
         q = (self.B, self.Nq, self.H, self.D)
         kv = (self.B, self.Nk, self.H, self.D)
-        if self.kind in ("dense", "block_causal"):
+        if self.kind in ("dense", "cross", "block_causal"):
             return [q, kv, kv]
         p = (self.B, self.Np, self.H, self.D)
         return [q, p, p, kv, kv]
@@ -88,12 +88,16 @@ class Workload:
         if self.kind == "dense":
             return (f"dense B={self.B} N={self.Nq} H={self.H} D={self.D} "
                     f"sigma={self.sigma}")
+        if self.kind == "cross":
+            return (f"cross B={self.B} Nq={self.Nq} Nk={self.Nk} H={self.H} D={self.D} "
+                    f"sigma={self.sigma}")
         return (f"prefix B={self.B} Nq=Nc={self.Nq} Np={self.Np} H={self.H} "
                 f"D={self.D} sigma={self.sigma}")
 
 
-# The five synthetic configurations.  1-3 and 5 are dense self-attention,
-# 4 is the prefix-cached form with a 1024-token prefix.  6 is the block-causal
+# The five synthetic configurations of the dense and prefix-cached forms:
+# 1-3 and 5 are dense self-attention, 4 is the prefix-cached form with a
+# 1024-token prefix.  6-8 cover the further forms.  6 is the block-causal
 # (empty-prefix) form of the same model's first evaluation: a text prompt, a
 # condition image, a short text run and the target image, each image a
 # contiguous block with its own id (definition prefix_cached_block_causal_h32_
@@ -107,6 +111,11 @@ WORKLOADS = {
     5: Workload(5, "dense_b1_n32768_h32_d128", "dense", 1, 32768, 32768, 32, 128, 0.5),
     6: Workload(6, "block_causal_b1_n4448_h32_d128", "block_causal", 1, 4448, 4448, 32, 128,
                 1.0, segments=((-1, 333), (0, 2048), (-1, 19), (1, 2048))),
+    # Cross attention (the dense definition's Nq != Nk case): video queries
+    # over a short conditioning sequence, and a short query block over a long
+    # context (fewer work units than SMs: the keys are split across SMs).
+    7: Workload(7, "cross_b1_nq8192_nk512_h32_d128", "cross", 1, 8192, 512, 32, 128, 1.0),
+    8: Workload(8, "cross_b1_nq256_nk32768_h32_d128", "cross", 1, 256, 32768, 32, 128, 1.0),
 }
 
 
