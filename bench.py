@@ -207,6 +207,12 @@ def make_call(ncp, w, dev_in, out):
     if w.kind == "cross":
         q, k, v = dev_in
         return lambda stream=None: ncp.attn_dense_cross_fwd(q, k, v, out, stream)
+    if w.kind == "masked_prefix":
+        q, kc, vc, kp, vp = dev_in
+        ids = workloads.image_ids(w).to(q.device)
+        valid = workloads.key_valid(w).to(q.device)
+        return lambda stream=None: ncp.attn_masked_prefix_fwd(q, kc, vc, kp, vp, ids, valid,
+                                                              w.sm_scale, out, stream)
     if w.kind == "block_causal":
         q, k, v = dev_in
         ids = workloads.image_ids(w).to(q.device)
@@ -297,6 +303,12 @@ def cpu_oracle_sample(w, inputs_cpu, target_s: float):
         fn = oracle.dense_attention_rows
     elif w.kind == "prefix":
         fn = oracle.prefix_attention_rows
+    elif w.kind == "masked_prefix":
+        ids = workloads.image_ids(w).numpy()
+        valid = workloads.key_valid(w).numpy().astype(np.uint8)
+        scale = float(np.float32(w.sm_scale))
+        fn = lambda *a: oracle.masked_prefix_attention_rows(  # noqa: E731
+            *a[:-1], ids, valid, scale, a[-1])
     else:
         ids = workloads.image_ids(w).numpy()
         fn = lambda *a: oracle.block_causal_attention_rows(*a[:-1], ids, a[-1])  # noqa: E731

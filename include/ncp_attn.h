@@ -112,6 +112,31 @@ int attn_block_causal_fwd(const void *q, const void *k, const void *v, const int
                           void *out, int B, int N, int H, int D, cudaStream_t stream);
 
 /*
+ * Masked prefix-cached attention: the earlier form of the definition
+ * definitions/block_causal_attention/prefix_cached_block_causal_h32_d128.json
+ * (field "reference" before the audit made every key visible).  Keys and
+ * values are cat(K_prefix, K_current) / cat(V_prefix, V_current); query i
+ * sits at position Np + i and sees key position j iff (j <= Np + i, or
+ * image_ids[Np + i] == image_ids[j] >= 0) and key_valid[b, j].  Scores are
+ * scaled by sm_scale (the old form's runtime scale).  Operand order is the
+ * old definition's: Q, K_current, V_current, K_prefix, V_prefix, image_ids,
+ * key_valid, sm_scale.
+ *   q, kc, vc:  [B, Nq, H, D] bf16, device, read only (Nc == Nq).
+ *   kp, vp:     [B, Np, H, D] bf16, device, read only (may be NULL when Np == 0).
+ *   image_ids:  [Np + Nq] int32, device, 16-byte aligned; -1 = text.
+ *   key_valid:  [B, Np + Nq] bytes (bool), device; 0 hides a key; NULL = all valid.
+ *   sm_scale:   finite, > 0.
+ *   out:        [B, Nq, H, D] bf16, device, written.
+ * Np + Nq <= 131072.  The definition requires every query to see at least
+ * one key; a row that sees none comes out as NaN.  Returns ATTN_OK or a
+ * negative attn_status (ATTN_ERR_SHAPE also for a bad sm_scale).
+ */
+int attn_masked_prefix_fwd(const void *q, const void *kc, const void *vc, const void *kp,
+                           const void *vp, const int *image_ids, const unsigned char *key_valid,
+                           float sm_scale, void *out, int B, int Nq, int Np, int H, int D,
+                           cudaStream_t stream);
+
+/*
  * attn_dense_fwd without any allocation, for callers that cannot call
  * cudaMalloc: an engine whose memory pool already owns the device memory, a
  * plugin that is handed only its input and output buffers, or a latency-bound

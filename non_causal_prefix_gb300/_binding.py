@@ -33,6 +33,8 @@ SIGNATURES = {
     "attn_dense_fwd_noalloc": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
     "attn_block_causal_fwd": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
     "attn_dense_cross_fwd": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
+    "attn_masked_prefix_fwd": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_float, _VP, _I, _I,
+                                    _I, _I, _I, _VP]),
 }
 
 _lock = threading.Lock()
@@ -182,6 +184,37 @@ def block_causal_attention(q, k, v, image_ids, stream=None):
     out = torch.empty_like(q)
     attn_block_causal_fwd(q, k, v, image_ids, out, stream)
     return out
+
+
+def attn_masked_prefix_fwd(q, kc, vc, kp, vp, image_ids, key_valid, sm_scale, out,
+                           stream=None) -> None:
+    """Enqueue the masked prefix-cached form: q, kc, vc, out [B, Nq, H, D]; kp, vp
+    [B, Np, H, D] (or None); image_ids int32 [Np + Nq]; key_valid bool/uint8
+    [B, Np + Nq] (or None: all valid); sm_scale > 0."""
+    import torch
+    B, Nq, H, D = _bnhd(q, "q")
+    for t, n in ((kc, "kc"), (vc, "vc"), (out, "out")):
+        if tuple(t.shape) != (B, Nq, H, D):
+            raise ValueError(f"{n} must have q's shape {tuple(q.shape)}")
+    Np = 0 if kp is None else kp.shape[1]
+    if Np > 0 and (tuple(kp.shape) != (B, Np, H, D) or tuple(vp.shape) != tuple(kp.shape)):
+        raise ValueError("kp/vp must be [B, Np, H, D] with q's B, H, D")
+    if image_ids.dtype != torch.int32 or not image_ids.is_cuda or not image_ids.is_contiguous():
+        raise ValueError("image_ids must be a contiguous CUDA int32 tensor")
+    if tuple(image_ids.shape) != (Np + Nq,):
+        raise ValueError("image_ids must be [Np + Nq]")
+    kv_ptr = None
+    if key_valid is not None:
+        if key_valid.dtype not in (torch.bool, torch.uint8) or not key_valid.is_cuda \
+                or not key_valid.is_contiguous() or tuple(key_valid.shape) != (B, Np + Nq):
+            raise ValueError("key_valid must be a contiguous CUDA bool/uint8 tensor [B, Np + Nq]")
+        kv_ptr = key_valid.data_ptr()
+    _check_tensors(*([q, kc, vc, out] + ([kp, vp] if Np > 0 else [])))
+    rc = load_library().attn_masked_prefix_fwd(
+        q.data_ptr(), kc.data_ptr(), vc.data_ptr(), kp.data_ptr() if Np > 0 else None,
+        vp.data_ptr() if Np > 0 else None, image_ids.data_ptr(), kv_ptr, float(sm_scale),
+        out.data_ptr(), B, Nq, Np, H, D, _stream_handle(stream))
+    _check(rc, "attn_masked_prefix_fwd")
 
 
 def _check_tensors(*ts):

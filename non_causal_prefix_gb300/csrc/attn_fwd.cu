@@ -110,7 +110,11 @@ struct Params {
   CUtensorMap tm_k[2];   // [0] prefix segment, [1] current segment
   CUtensorMap tm_v[2];
   __nv_bfloat16* out;
-  const int* image_ids;  // block-causal form: [Nq] image id per token, -1 = text
+  // Masked forms (block-causal, masked prefix-cached): image id per key
+  // position [Np + Nq] (-1 = text) and, optionally, key_valid [B, Np + Nq]
+  // (nullptr: every key valid).  Query i sits at position Np + i.
+  const int* image_ids;
+  const unsigned char* key_valid;
   int Nq, H;
   int q_pairs;           // ceil(Nq / 256): units per (b, h); units are (b, h, q pair), q pair fastest
   // Work items, walked round-robin by the persistent CTAs: items [0, n_whole)
@@ -469,32 +473,52 @@ struct TileTable {
   const int* uni;
 };
 
+// Key tiles walk the prefix segment (tiles [0, T0)) then the current one;
+// position of the first key of tile t, and its number of keys.
+__device__ __forceinline__ int key_tile_pos(const Params& p, int t) {
+  const int T0 = p.n_tiles[0];
+  return t < T0 ? t * BN : p.n_tok[0] + (t - T0) * BN;
+}
+__device__ __forceinline__ int key_tile_len(const Params& p, int t) {
+  const int T0 = p.n_tiles[0];
+  const int seg = t < T0 ? 0 : 1;
+  return min(BN, p.n_tok[seg] - (t - (seg ? T0 : 0)) * BN);
+}
+
 // Some query row of the unit sees some key of tile t: causally (the tile
-// starts at or before the unit's last row), or through an image id both may
-// share (their id ranges meet).  Exact as a filter: a skipped tile has no
-// visible pair.
-__device__ __forceinline__ bool bc_unit_visits(const TileTable& tt, const Unit& u, int N, int t) {
-  const int r_last = min(u.q0 + 2 * BM, N) - 1;
-  if (t * BN <= r_last) return true;
-  const int qt0 = u.q0 / BM;
+// starts at or before the unit's last row, at position Np + row), or through
+// an image id both may share (their id ranges meet; the query tiles are the
+// current segment's tiles T0 + qt).  key_valid only removes keys, so the
+// filter stays exact: a skipped tile has no visible pair.
+__device__ __forceinline__ bool bc_unit_visits(const TileTable& tt, const Params& p, const Unit& u,
+                                               int t) {
+  const int r_last = p.n_tok[0] + min(u.q0 + 2 * BM, p.Nq) - 1;
+  if (key_tile_pos(p, t) <= r_last) return true;
+  const int qt0 = p.n_tiles[0] + u.q0 / BM;
   const int qt1 = u.two ? qt0 + 1 : qt0;
   const int qlo = min(tt.lo[qt0], tt.lo[qt1]);
   const int qhi = max(tt.hi[qt0], tt.hi[qt1]);
   return qlo <= tt.hi[t] && tt.lo[t] <= qhi;
 }
 
-// Every query row of query tile qt (first row q_first) sees every key of tile
-// t: the keys all precede the rows, or both tiles hold one and the same image.
-__device__ __forceinline__ bool bc_tile_full(const TileTable& tt, int qt, int q_first, int t) {
-  if (t * BN + BN - 1 <= q_first) return true;
-  return tt.uni[qt] && tt.uni[t] && tt.lo[qt] == tt.lo[t];
+// Every query row of query tile qt (current-segment tile T0 + qt, first row
+// q_first) sees every key of tile t through causality or one shared image
+// (key_valid aside): the keys all precede the rows, or both tiles hold one
+// and the same image.
+__device__ __forceinline__ bool bc_tile_full(const TileTable& tt, const Params& p, int qt,
+                                             int q_first, int t) {
+  if (key_tile_pos(p, t) + key_tile_len(p, t) - 1 <= p.n_tok[0] + q_first) return true;
+  const int tq = p.n_tiles[0] + qt;
+  return tt.uni[tq] && tt.uni[t] && tt.lo[tq] == tt.lo[t];
 }
 
-// Per-row mask of one key tile of the block-causal form: key c0 + c is visible
-// to query row qi (image id idq) iff c0 + c <= qi or its id equals idq >= 0.
+// Per-row mask of one key tile of the masked forms: key position c0 + c is
+// visible to the query at position qi (image id idq) iff c0 + c <= qi or its
+// id equals idq >= 0, and (with key_valid) the key is valid.
 struct RowMask {
   const int* ids;  // image ids of the tile's keys (ids[0] is key c0); nullptr: all visible
-  int c0, qi, idq, n;  // n: keys of the sequence (ids past n are not read)
+  const unsigned char* valid;  // key_valid of the tile's keys for this batch; nullptr: all valid
+  int c0, qi, idq, n;  // n: key positions (Np + Nq; nothing past n is read)
 };
 
 // One 128-key tile of the online softmax for this thread's query row:
@@ -520,7 +544,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, i
   }
   if (BC && mask.ids) {
     const int lim = mask.qi - mask.c0;  // keys c <= lim are visible causally
-    if (mask.c0 + BN <= mask.n) {
+    if (mask.c0 + BN <= mask.n && (mask.c0 & 3) == 0) {
       const int4* ids4 = reinterpret_cast<const int4*>(mask.ids);
 #pragma unroll
       for (int c = 0; c < BN; c += 4) {
@@ -532,13 +556,19 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, i
         if (!(c + 3 <= lim || (img && id.w == mask.idq))) s[c + 3] = -INFINITY;
       }
     } else {
-      // Last tile of the sequence: keys past n are already masked (valid).
+      // Last tile of the sequence, or ids not 16-byte aligned: one by one.
+      // Keys past n are already masked (valid).
 #pragma unroll
       for (int c = 0; c < BN; ++c) {
         const int id = (mask.c0 + c < mask.n) ? __ldg(mask.ids + c) : -1;
         if (!(c <= lim || (mask.idq >= 0 && id == mask.idq))) s[c] = -INFINITY;
       }
     }
+  }
+  if (BC && mask.valid) {
+#pragma unroll
+    for (int c = 0; c < BN; ++c)
+      if (mask.c0 + c < mask.n && __ldg(mask.valid + c) == 0) s[c] = -INFINITY;
   }
   // Row maximum: four independent chains of 3-input max.
   float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
@@ -683,19 +713,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // Block-causal form: summarise the image ids of every 128-token tile.
-  const int n_seq = p.Nq;
+  // Masked forms: summarise the image ids of every key tile.
+  const int n_all = p.n_tok[0] + p.n_tok[1];
   TileTable tt{nullptr, nullptr, nullptr};
   if constexpr (BC) {
     int* t_lo = reinterpret_cast<int*>(base + C::SUM_OFF);
     int* t_hi = t_lo + MAX_SEQ_TILES;
     int* t_uni = t_hi + MAX_SEQ_TILES;
-    for (int t = warp; t < p.n_tiles[1]; t += NUM_THREADS / 32) {
+    for (int t = warp; t < T; t += NUM_THREADS / 32) {
       int lo = 0x7fffffff, hi = -1;
       bool text = false;
+      const int pos0 = key_tile_pos(p, t), len = key_tile_len(p, t);
       for (int e = lane; e < BN; e += 32) {
-        const int j = t * BN + e;
-        if (j < n_seq) {
+        const int j = pos0 + e;
+        if (e < len) {
           const int id = __ldg(p.image_ids + j);
           if (id < 0) {
             text = true;
@@ -752,7 +783,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         u.q0 + i * BM, u.b, bar_q);
         q_last = n;
         for (int t = it.t_begin; t < it.t_end && ok; ++t) {
-          if (BC && !bc_unit_visits(tt, u, n_seq, t)) continue;
+          if (BC && !bc_unit_visits(tt, p, u, t)) continue;
           const int seg = (t < T0) ? 0 : 1;
           const int tok0 = (t - (seg ? T0 : 0)) * BN;
           for (int kind = 0; kind < 2; ++kind) {
@@ -828,7 +859,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int v_prev = -1;
         int j = 0;  // key tiles visited so far in this item
         for (int t = it.t_begin; t < it.t_end && ok; ++t) {
-          if (BC && !bc_unit_visits(tt, it.u, n_seq, t)) continue;
+          if (BC && !bc_unit_visits(tt, p, it.u, t)) continue;
           const int k_slot = slot;
           ok = wait_bounded(bar_kv_full(k_slot), phase, limit, abort_flag, 3);
           if (!ok) break;
@@ -885,18 +916,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (i == 1 && !u.two) continue;
       float m = -INFINITY;  // running (possibly stale) maximum, log2 units
       float l = 0.f;        // running sum of exp2(x - m)
-      RowMask mask{nullptr, 0, 0, -1, n_seq};
+      RowMask mask{nullptr, nullptr, 0, 0, -1, n_all};
       if constexpr (BC) {
-        mask.qi = u.q0 + i * BM + row;
-        mask.idq = mask.qi < n_seq ? __ldg(p.image_ids + mask.qi) : -1;
+        const int qrow = u.q0 + i * BM + row;  // query index; past Nq: a padding row
+        mask.qi = p.n_tok[0] + qrow;
+        mask.idq = qrow < p.Nq ? __ldg(p.image_ids + mask.qi) : -1;
       }
       int j = 0;  // key tiles visited so far in this item
       for (int t = it.t_begin; t < it.t_end; ++t) {
         if constexpr (BC) {
-          if (!bc_unit_visits(tt, u, n_seq, t)) continue;
-          const bool full = bc_tile_full(tt, u.q0 / BM + i, u.q0 + i * BM, t);
-          mask.ids = full ? nullptr : p.image_ids + t * BN;
-          mask.c0 = t * BN;
+          if (!bc_unit_visits(tt, p, u, t)) continue;
+          const bool full = bc_tile_full(tt, p, u.q0 / BM + i, u.q0 + i * BM, t);
+          mask.c0 = key_tile_pos(p, t);
+          mask.ids = full ? nullptr : p.image_ids + mask.c0;
+          mask.valid = p.key_valid ? p.key_valid + static_cast<size_t>(u.b) * n_all + mask.c0
+                                   : nullptr;
         }
         ok = warp_wait(bar_s[i], sc & 1u, limit, abort_flag, 7);
         if (!ok) break;
@@ -1231,8 +1265,8 @@ int launch(Params& prm, long long n_units, cudaStream_t stream) {
 
 // Argument checks, TMA descriptors and kernel parameters of one call.
 int prepare(const void* q, const void* kp, const void* vp, const void* kc, const void* vc,
-            const int* image_ids, void* out, int B, int Nq, int Np, int Nc, int H, int D,
-            Params& prm, long long& n_units) {
+            const int* image_ids, const unsigned char* key_valid, float sm_scale, void* out, int B,
+            int Nq, int Np, int Nc, int H, int D, Params& prm, long long& n_units) {
   if (!q || !kc || !vc || !out || (Np > 0 && (!kp || !vp))) return ATTN_ERR_NULL;
   if (B < 1 || Nq < 1 || Nc < 1 || H < 1 || Np < 0) return ATTN_ERR_SHAPE;
   if (H > 65535 || B > 65535) return ATTN_ERR_SHAPE;
@@ -1264,6 +1298,7 @@ int prepare(const void* q, const void* kp, const void* vp, const void* kc, const
   if (n_units > 0x7fffffffLL) return ATTN_ERR_SHAPE;
   prm.out = static_cast<__nv_bfloat16*>(out);
   prm.image_ids = image_ids;
+  prm.key_valid = key_valid;
   prm.Nq = Nq;
   prm.H = H;
   prm.q_pairs = static_cast<int>(q_pairs);
@@ -1271,7 +1306,10 @@ int prepare(const void* q, const void* kp, const void* vp, const void* kc, const
   prm.n_tok[1] = Nc;
   prm.n_tiles[0] = (Np + ncp::BN - 1) / ncp::BN;
   prm.n_tiles[1] = (Nc + ncp::BN - 1) / ncp::BN;
-  prm.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+  // Scale D^-0.5 unless the call passes one (sm_scale > 0), times log2(e).
+  const double scale = sm_scale > 0.f ? static_cast<double>(sm_scale)
+                                      : 1.0 / std::sqrt(static_cast<double>(D));
+  prm.scale_log2 = static_cast<float>(1.4426950408889634 * scale);
   {
     std::lock_guard<std::mutex> lock(g_cfg_mutex);
     prm.fault_mode = g_fault_mode;
@@ -1351,11 +1389,12 @@ int launch_noalloc(Params& prm, long long n_units, cudaStream_t stream) {
 }
 
 int run(const void* q, const void* kp, const void* vp, const void* kc, const void* vc,
-        const int* image_ids, void* out, int B, int Nq, int Np, int Nc, int H, int D,
-        cudaStream_t stream) {
+        const int* image_ids, const unsigned char* key_valid, float sm_scale, void* out, int B,
+        int Nq, int Np, int Nc, int H, int D, cudaStream_t stream) {
   Params prm;
   long long n_units = 0;
-  const int rc = prepare(q, kp, vp, kc, vc, image_ids, out, B, Nq, Np, Nc, H, D, prm, n_units);
+  const int rc = prepare(q, kp, vp, kc, vc, image_ids, key_valid, sm_scale, out, B, Nq, Np, Nc, H,
+                         D, prm, n_units);
   if (rc != ATTN_OK) return rc;
   if (image_ids)
     return D == 128 ? launch<128, true>(prm, n_units, stream)
@@ -1371,13 +1410,33 @@ extern "C" {
 int attn_dense_fwd(const void* q, const void* k, const void* v, void* out, int B, int N, int H,
                    int D, cudaStream_t stream) {
   if (!k || !v) return ATTN_ERR_NULL;
-  return run(q, nullptr, nullptr, k, v, nullptr, out, B, N, 0, N, H, D, stream);
+  return run(q, nullptr, nullptr, k, v, nullptr, nullptr, 0.f, out, B, N, 0, N, H, D, stream);
 }
 
 int attn_dense_cross_fwd(const void* q, const void* k, const void* v, void* out, int B, int Nq,
                          int Nk, int H, int D, cudaStream_t stream) {
   if (!k || !v) return ATTN_ERR_NULL;
-  return run(q, nullptr, nullptr, k, v, nullptr, out, B, Nq, 0, Nk, H, D, stream);
+  return run(q, nullptr, nullptr, k, v, nullptr, nullptr, 0.f, out, B, Nq, 0, Nk, H, D, stream);
+}
+
+int attn_masked_prefix_fwd(const void* q, const void* kc, const void* vc, const void* kp,
+                           const void* vp, const int* image_ids, const unsigned char* key_valid,
+                           float sm_scale, void* out, int B, int Nq, int Np, int H, int D,
+                           cudaStream_t stream) {
+  if (!kc || !vc || !image_ids) return ATTN_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(image_ids) & 15u) != 0) return ATTN_ERR_ALIGN;
+  if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return ATTN_ERR_SHAPE;
+  if (Np < 0 || Nq < 1 || static_cast<long long>(Np) + Nq > ncp::MAX_SEQ_TILES * ncp::BN ||
+      (Np + ncp::BN - 1) / ncp::BN + (Nq + ncp::BN - 1) / ncp::BN > ncp::MAX_SEQ_TILES)
+    return ATTN_ERR_SHAPE;
+  const size_t n_all = static_cast<size_t>(Np) + Nq;
+  if (B >= 1 && H >= 1 && D >= 1) {
+    const size_t o_bytes = static_cast<size_t>(B) * Nq * H * D * 2;
+    if (overlaps(out, o_bytes, image_ids, n_all * sizeof(int)) ||
+        (key_valid && overlaps(out, o_bytes, key_valid, static_cast<size_t>(B) * n_all)))
+      return ATTN_ERR_ALIAS;
+  }
+  return run(q, kp, vp, kc, vc, image_ids, key_valid, sm_scale, out, B, Nq, Np, Nq, H, D, stream);
 }
 
 int attn_block_causal_fwd(const void* q, const void* k, const void* v, const int* image_ids,
@@ -1389,7 +1448,7 @@ int attn_block_causal_fwd(const void* q, const void* k, const void* v, const int
       overlaps(out, static_cast<size_t>(B) * N * H * D * 2, image_ids,
                static_cast<size_t>(N) * sizeof(int)))
     return ATTN_ERR_ALIAS;
-  return run(q, nullptr, nullptr, k, v, image_ids, out, B, N, 0, N, H, D, stream);
+  return run(q, nullptr, nullptr, k, v, image_ids, nullptr, 0.f, out, B, N, 0, N, H, D, stream);
 }
 
 int attn_dense_fwd_noalloc(const void* q, const void* k, const void* v, void* out, int B, int N,
@@ -1397,7 +1456,8 @@ int attn_dense_fwd_noalloc(const void* q, const void* k, const void* v, void* ou
   if (!k || !v) return ATTN_ERR_NULL;
   Params prm;
   long long n_units = 0;
-  const int rc = prepare(q, nullptr, nullptr, k, v, nullptr, out, B, N, 0, N, H, D, prm, n_units);
+  const int rc =
+      prepare(q, nullptr, nullptr, k, v, nullptr, nullptr, 0.f, out, B, N, 0, N, H, D, prm, n_units);
   if (rc != ATTN_OK) return rc;
   return D == 128 ? launch_noalloc<128>(prm, n_units, stream)
                   : launch_noalloc<64>(prm, n_units, stream);
@@ -1405,7 +1465,7 @@ int attn_dense_fwd_noalloc(const void* q, const void* k, const void* v, void* ou
 
 int attn_prefix_fwd(const void* q, const void* kp, const void* vp, const void* kc, const void* vc,
                     void* out, int B, int Nq, int Np, int Nc, int H, int D, cudaStream_t stream) {
-  return run(q, kp, vp, kc, vc, nullptr, out, B, Nq, Np, Nc, H, D, stream);
+  return run(q, kp, vp, kc, vc, nullptr, nullptr, 0.f, out, B, Nq, Np, Nc, H, D, stream);
 }
 
 const char* attn_status_string(int status) {

@@ -4,14 +4,16 @@ Only the tests, ``__graft_entry__.smoke()`` and the bench's CPU-baseline leg
 import this package.  The product path (``non_causal_prefix_gb300``) never
 does, and this package never imports the product path.
 
-The arithmetic lives in ``attn_oracle.c`` (dense and prefix-cached forms) and
-``attn_oracle_block_causal.c`` (plain C, FP64, OpenMP over output rows); this
-module only compiles them with gcc into one library and marshals numpy arrays.
+The arithmetic lives in ``attn_oracle.c`` (dense and prefix-cached forms),
+``attn_oracle_block_causal.c`` and ``attn_oracle_masked_prefix.c`` (plain C,
+FP64, OpenMP over output rows); this module only compiles them with gcc into
+one library and marshals numpy arrays.
 Inputs are bf16 bit patterns (``numpy.uint16``, layout ``[B, N, H, D]``);
 outputs are float64 ``[B, Nq, H, D]`` (or ``[rows, D]`` for sampled rows).
 
 Pins: the dense and prefix functions are checked in ``tests/test_oracle.py``,
-the block-causal ones in ``tests/test_oracle_block_causal.py``, against
+the block-causal ones in ``tests/test_oracle_block_causal.py``, the masked
+prefix ones in ``tests/test_oracle_masked_prefix.py``, against
 closed forms (one key; identical keys; one dominant logit; the two-key
 logistic weight), invariants (joint K/V permutation, query/head/batch
 independence, prefix == dense on the explicit concatenation), a pure-Python
@@ -29,7 +31,8 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 SOURCE = os.path.join(_HERE, "attn_oracle.c")
 SOURCE_BLOCK_CAUSAL = os.path.join(_HERE, "attn_oracle_block_causal.c")
-SOURCES = [SOURCE, SOURCE_BLOCK_CAUSAL]
+SOURCE_MASKED_PREFIX = os.path.join(_HERE, "attn_oracle_masked_prefix.c")
+SOURCES = [SOURCE, SOURCE_BLOCK_CAUSAL, SOURCE_MASKED_PREFIX]
 _LIB_DIR = os.path.join(_HERE, "_lib")
 _LIB = os.path.join(_LIB_DIR, "liboracle.so")
 _lock = threading.Lock()
@@ -103,6 +106,17 @@ class Oracle:
                 u16p, u16p, u16p, i32p, f64p, ci, ci, ci, ci, i64p, ctypes.c_int64]
             lib.oracle_block_causal_attention.restype = ci
             lib.oracle_block_causal_attention_rows.restype = ci
+        if hasattr(lib, "oracle_masked_prefix_attention"):
+            i32p = ctypes.POINTER(ctypes.c_int32)
+            u8p = ctypes.POINTER(ctypes.c_uint8)
+            cf = ctypes.c_float
+            lib.oracle_masked_prefix_attention.argtypes = [
+                u16p, u16p, u16p, u16p, u16p, i32p, u8p, cf, f64p, ci, ci, ci, ci, ci]
+            lib.oracle_masked_prefix_attention_rows.argtypes = [
+                u16p, u16p, u16p, u16p, u16p, i32p, u8p, cf, f64p, ci, ci, ci, ci, ci, i64p,
+                ctypes.c_int64]
+            lib.oracle_masked_prefix_attention.restype = ci
+            lib.oracle_masked_prefix_attention_rows.restype = ci
         lib.oracle_set_threads.argtypes = [ci]
         lib.oracle_set_threads.restype = None
         self.lib = lib
@@ -219,6 +233,56 @@ class Oracle:
             _ptr(rows, ctypes.c_int64), rows.size), "oracle_block_causal_attention_rows")
         return out
 
+    def _masked_prefix_args(self, Q, K_current, V_current, K_prefix, V_prefix, image_ids,
+                            key_valid):
+        Q, Kc, Vc = _u16(Q), _u16(K_current), _u16(V_current)
+        B, Nq, H, D = Q.shape
+        if Kc.shape != Q.shape or Vc.shape != Q.shape:
+            raise ValueError("Q, K_current, V_current must all be [B, Nq, H, D]")
+        Np = 0 if K_prefix is None else K_prefix.shape[1]
+        if Np > 0:
+            Kp, Vp = _u16(K_prefix), _u16(V_prefix)
+            if Kp.shape != (B, Np, H, D) or Vp.shape != Kp.shape:
+                raise ValueError("K_prefix/V_prefix must be [B, Np, H, D]")
+            pk, pv = _ptr(Kp, ctypes.c_uint16), _ptr(Vp, ctypes.c_uint16)
+        else:
+            Kp = Vp = None
+            pk = pv = ctypes.POINTER(ctypes.c_uint16)()
+        ids = np.ascontiguousarray(image_ids, dtype=np.int32)
+        valid = np.ascontiguousarray(key_valid, dtype=np.uint8)
+        if ids.shape != (Np + Nq,) or valid.shape != (B, Np + Nq):
+            raise ValueError("image_ids must be [Np + Nq] and key_valid [B, Np + Nq]")
+        keep = (Q, Kc, Vc, Kp, Vp, ids, valid)
+        return keep, (pk, pv), (B, Nq, Np, H, D)
+
+    def masked_prefix_attention(self, Q, K_current, V_current, K_prefix, V_prefix, image_ids,
+                                key_valid, sm_scale) -> np.ndarray:
+        """Masked prefix-cached attention in FP64 (the pre-audit prefix form)."""
+        keep, (pk, pv), (B, Nq, Np, H, D) = self._masked_prefix_args(
+            Q, K_current, V_current, K_prefix, V_prefix, image_ids, key_valid)
+        Q, Kc, Vc, _, _, ids, valid = keep
+        out = np.empty((B, Nq, H, D), dtype=np.float64)
+        _check(self.lib.oracle_masked_prefix_attention(
+            _ptr(Q, ctypes.c_uint16), _ptr(Kc, ctypes.c_uint16), _ptr(Vc, ctypes.c_uint16), pk, pv,
+            _ptr(ids, ctypes.c_int32), _ptr(valid, ctypes.c_uint8), float(sm_scale),
+            _ptr(out, ctypes.c_double), B, Nq, Np, H, D), "oracle_masked_prefix_attention")
+        return out
+
+    def masked_prefix_attention_rows(self, Q, K_current, V_current, K_prefix, V_prefix, image_ids,
+                                     key_valid, sm_scale, rows) -> np.ndarray:
+        """Sampled rows of ``masked_prefix_attention`` (flat row r = (b*Nq + i)*H + h)."""
+        keep, (pk, pv), (B, Nq, Np, H, D) = self._masked_prefix_args(
+            Q, K_current, V_current, K_prefix, V_prefix, image_ids, key_valid)
+        Q, Kc, Vc, _, _, ids, valid = keep
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        out = np.empty((rows.size, D), dtype=np.float64)
+        _check(self.lib.oracle_masked_prefix_attention_rows(
+            _ptr(Q, ctypes.c_uint16), _ptr(Kc, ctypes.c_uint16), _ptr(Vc, ctypes.c_uint16), pk, pv,
+            _ptr(ids, ctypes.c_int32), _ptr(valid, ctypes.c_uint8), float(sm_scale),
+            _ptr(out, ctypes.c_double), B, Nq, Np, H, D, _ptr(rows, ctypes.c_int64), rows.size),
+            "oracle_masked_prefix_attention_rows")
+        return out
+
 
 def default() -> Oracle:
     """The oracle compiled from ``attn_oracle.c`` (built on first use)."""
@@ -259,3 +323,15 @@ def block_causal_attention(Q, K, V, image_ids) -> np.ndarray:
 
 def block_causal_attention_rows(Q, K, V, image_ids, rows) -> np.ndarray:
     return default().block_causal_attention_rows(Q, K, V, image_ids, rows)
+
+
+def masked_prefix_attention(Q, K_current, V_current, K_prefix, V_prefix, image_ids, key_valid,
+                            sm_scale) -> np.ndarray:
+    return default().masked_prefix_attention(Q, K_current, V_current, K_prefix, V_prefix,
+                                             image_ids, key_valid, sm_scale)
+
+
+def masked_prefix_attention_rows(Q, K_current, V_current, K_prefix, V_prefix, image_ids, key_valid,
+                                 sm_scale, rows) -> np.ndarray:
+    return default().masked_prefix_attention_rows(Q, K_current, V_current, K_prefix, V_prefix,
+                                                  image_ids, key_valid, sm_scale, rows)

@@ -38,8 +38,12 @@ class Workload:
     D: int
     sigma: float
     Np: int = 0      # prefix length (prefix form only)
-    # Block-causal form: the token sequence as (image id, length) runs; -1 = text.
+    # Block-causal and masked prefix forms: the key positions as (image id,
+    # length) runs; -1 = text.
     segments: tuple = ()
+    # Masked prefix form: runtime scale and [start, end) runs of padded keys.
+    sm_scale: float = 0.0
+    invalid: tuple = ()
 
     @property
     def n_keys(self) -> int:
@@ -49,6 +53,18 @@ class Workload:
     @property
     def visible_pairs(self) -> int:
         """(query, key) pairs that enter the softmax, per (batch, head)."""
+        if self.kind == "masked_prefix":
+            ids = np.concatenate([np.full(n, k, dtype=np.int64) for k, n in self.segments])
+            valid = np.ones(ids.size, dtype=bool)
+            for a, b in self.invalid:
+                valid[a:b] = False
+            j = np.arange(ids.size)
+            total = 0
+            for i in range(self.Nq):
+                qp = self.Np + i
+                vis = (j <= qp) | ((ids[qp] >= 0) & (ids == ids[qp]))
+                total += int(np.count_nonzero(vis & valid))
+            return total
         if self.kind != "block_causal":
             return self.Nq * self.n_keys
         total, pos = 0, 0
@@ -77,6 +93,9 @@ class Workload:
         kv = (self.B, self.Nk, self.H, self.D)
         if self.kind in ("dense", "cross", "block_causal"):
             return [q, kv, kv]
+        if self.kind == "masked_prefix":   # the old definition's operand order
+            p = (self.B, self.Np, self.H, self.D)
+            return [q, q, q, p, p]
         p = (self.B, self.Np, self.H, self.D)
         return [q, p, p, kv, kv]
 
@@ -88,6 +107,9 @@ class Workload:
         if self.kind == "dense":
             return (f"dense B={self.B} N={self.Nq} H={self.H} D={self.D} "
                     f"sigma={self.sigma}")
+        if self.kind == "masked_prefix":
+            return (f"masked prefix B={self.B} Nq={self.Nq} Np={self.Np} H={self.H} D={self.D} "
+                    f"padding={list(self.invalid)} sm_scale={self.sm_scale:.6g}")
         if self.kind == "cross":
             return (f"cross B={self.B} Nq={self.Nq} Nk={self.Nk} H={self.H} D={self.D} "
                     f"sigma={self.sigma}")
@@ -116,6 +138,12 @@ WORKLOADS = {
     # context (fewer work units than SMs: the keys are split across SMs).
     7: Workload(7, "cross_b1_nq8192_nk512_h32_d128", "cross", 1, 8192, 512, 32, 128, 1.0),
     8: Workload(8, "cross_b1_nq256_nk32768_h32_d128", "cross", 1, 256, 32768, 32, 128, 1.0),
+    # The pre-audit prefix form: a 1024-token prefix (a 256-token prompt whose
+    # last 56 tokens are padding, then a 768-token condition image) and a
+    # 4096-token target image as the current block; runtime scale 128^-0.5.
+    9: Workload(9, "masked_prefix_b1_nq4096_np1024_h32_d128", "masked_prefix", 1, 4096, 4096, 32,
+                128, 1.0, Np=1024, segments=((-1, 256), (0, 768), (1, 4096)),
+                sm_scale=128 ** -0.5, invalid=((200, 256),)),
 }
 
 
@@ -141,6 +169,14 @@ def custom(kind: str, B: int, Nq: int, Nk: int, H: int, D: int, sigma: float = 1
     if segments:
         assert sum(n for _, n in segments) == Nq == Nk
     return Workload(config_id, name, kind, B, Nq, Nk, H, D, sigma, Np=Np, segments=segments)
+
+
+def key_valid(w: Workload) -> torch.Tensor:
+    """The [B, Np + Nq] key-valid mask of a masked prefix workload (CPU bool)."""
+    valid = torch.ones((w.B, w.Np + w.Nq), dtype=torch.bool)
+    for a, b in w.invalid:
+        valid[:, a:b] = False
+    return valid
 
 
 def image_ids(w: Workload) -> torch.Tensor:
