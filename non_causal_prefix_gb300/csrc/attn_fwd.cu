@@ -566,9 +566,32 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, i
     }
   }
   if (BC && mask.valid) {
+    if (mask.c0 + BN <= mask.n && (reinterpret_cast<uintptr_t>(mask.valid) & 15u) == 0) {
+      // 128 flags as eight 16-byte loads; the per-key pass (loading them
+      // again) runs only when a flag is zero (zero-byte test per word).
+      const uint4* kv4 = reinterpret_cast<const uint4*>(mask.valid);
+      uint32_t zero = 0;
 #pragma unroll
-    for (int c = 0; c < BN; ++c)
-      if (mask.c0 + c < mask.n && __ldg(mask.valid + c) == 0) s[c] = -INFINITY;
+      for (int k = 0; k < 8; ++k) {
+        const uint4 v = __ldg(kv4 + k);
+        zero |= ((v.x - 0x01010101u) & ~v.x) | ((v.y - 0x01010101u) & ~v.y) |
+                ((v.z - 0x01010101u) & ~v.z) | ((v.w - 0x01010101u) & ~v.w);
+      }
+      if (zero & 0x80808080u) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 v = __ldg(kv4 + k);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            if (((w[c / 4] >> (8 * (c % 4))) & 0xffu) == 0) s[16 * k + c] = -INFINITY;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < BN; ++c)
+        if (mask.c0 + c < mask.n && __ldg(mask.valid + c) == 0) s[c] = -INFINITY;
+    }
   }
   // Row maximum: four independent chains of 3-input max.
   float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
