@@ -422,10 +422,13 @@ struct Unit {
 template <bool BC>
 __device__ __forceinline__ Unit decode_unit(const Params& p, int unit) {
   Unit u;
-  // Block-causal rows see more keys the later they sit: hand out the last
-  // query pairs first (longest work first).
-  const int qp = BC ? p.q_pairs - 1 - unit % p.q_pairs : unit % p.q_pairs;
-  const int bh = unit / p.q_pairs;
+  // Dense forms: query pair fastest, so the CTAs running at one time share
+  // the K/V of a few heads in L2.  Masked forms: rows see more keys the later
+  // they sit, so hand out the last query pairs first, over all heads (longest
+  // work first; all heads' K/V stay in L2 at these lengths).
+  const int n_bh = p.H * (p.n_items / (p.q_pairs * p.H));  // B * H (masked forms never split)
+  const int qp = BC ? p.q_pairs - 1 - unit / n_bh : unit % p.q_pairs;
+  const int bh = BC ? unit % n_bh : unit / p.q_pairs;
   u.h = bh % p.H;
   u.b = bh / p.H;
   u.q0 = qp * (2 * BM);
@@ -439,6 +442,15 @@ struct Item {
   int split;           // -1: whole unit; else index of the split unit
   int piece;
 };
+
+// The n-th item of this CTA.  Dense forms: round robin.  Masked forms (units
+// of unequal work, longest first): a snake, so that CTAs that took a long
+// unit in one round take a short one in the next.
+template <bool BC>
+__device__ __forceinline__ int item_at(int n) {
+  const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return n * g + ((BC && (n & 1)) ? g - 1 - c : c);
+}
 
 template <bool BC>
 __device__ __forceinline__ Item decode_item(const Params& p, int item, int T) {
@@ -528,6 +540,71 @@ template <int D, bool BC>
 __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, int valid, float sl2,
                                              bool may_rescale, const RowMask& mask, float& m,
                                              float& l) {
+  // Masked forms: this row's visibility of the tile's 128 keys as a bitmask,
+  // built before the scores are loaded so that fewer registers are live.
+  uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
+  bool masked = false;
+  if (BC && mask.ids) {
+    masked = true;
+    const int lim = mask.qi - mask.c0;  // keys c <= lim are visible causally
+    const bool img = mask.idq >= 0;
+    if (mask.c0 + BN <= mask.n && (mask.c0 & 3) == 0) {
+      const int4* ids4 = reinterpret_cast<const int4*>(mask.ids);
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        uint32_t w = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int4 id = __ldg(ids4 + 8 * g + k);
+          const int c = 32 * g + 4 * k;
+          w |= static_cast<uint32_t>(c + 0 <= lim || (img && id.x == mask.idq)) << (4 * k + 0);
+          w |= static_cast<uint32_t>(c + 1 <= lim || (img && id.y == mask.idq)) << (4 * k + 1);
+          w |= static_cast<uint32_t>(c + 2 <= lim || (img && id.z == mask.idq)) << (4 * k + 2);
+          w |= static_cast<uint32_t>(c + 3 <= lim || (img && id.w == mask.idq)) << (4 * k + 3);
+        }
+        vis[g] = w;
+      }
+    } else {
+      // Last tile of the sequence, or ids not 16-byte aligned: one by one.
+      // Keys past n are masked by `valid` below.
+#pragma unroll
+      for (int c = 0; c < BN; ++c) {
+        const int id = (mask.c0 + c < mask.n) ? __ldg(mask.ids + c) : -1;
+        if (!(c <= lim || (img && id == mask.idq))) vis[c / 32] &= ~(1u << (c % 32));
+      }
+    }
+  }
+  if (BC && mask.valid) {
+    if (mask.c0 + BN <= mask.n && (reinterpret_cast<uintptr_t>(mask.valid) & 15u) == 0) {
+      // 128 flags as eight 16-byte loads; the per-key pass runs only when a
+      // flag is zero (zero-byte test per 32-bit word).
+      const uint4* kv4 = reinterpret_cast<const uint4*>(mask.valid);
+      uint32_t zero = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint4 v = __ldg(kv4 + k);
+        zero |= ((v.x - 0x01010101u) & ~v.x) | ((v.y - 0x01010101u) & ~v.y) |
+                ((v.z - 0x01010101u) & ~v.z) | ((v.w - 0x01010101u) & ~v.w);
+      }
+      if (zero & 0x80808080u) {
+        masked = true;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 v = __ldg(kv4 + k);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            if (((w[c / 4] >> (8 * (c % 4))) & 0xffu) == 0)
+              vis[(16 * k + c) / 32] &= ~(1u << ((16 * k + c) % 32));
+        }
+      }
+    } else {
+      masked = true;
+#pragma unroll
+      for (int c = 0; c < BN; ++c)
+        if (mask.c0 + c < mask.n && __ldg(mask.valid + c) == 0) vis[c / 32] &= ~(1u << (c % 32));
+    }
+  }
   float s[BN];
   {
     uint32_t r[BN];
@@ -542,56 +619,10 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, i
     for (int c = 0; c < BN; ++c)
       if (c >= valid) s[c] = -INFINITY;
   }
-  if (BC && mask.ids) {
-    const int lim = mask.qi - mask.c0;  // keys c <= lim are visible causally
-    if (mask.c0 + BN <= mask.n && (mask.c0 & 3) == 0) {
-      const int4* ids4 = reinterpret_cast<const int4*>(mask.ids);
+  if (BC && masked) {
 #pragma unroll
-      for (int c = 0; c < BN; c += 4) {
-        const int4 id = __ldg(ids4 + c / 4);
-        const bool img = mask.idq >= 0;
-        if (!(c + 0 <= lim || (img && id.x == mask.idq))) s[c + 0] = -INFINITY;
-        if (!(c + 1 <= lim || (img && id.y == mask.idq))) s[c + 1] = -INFINITY;
-        if (!(c + 2 <= lim || (img && id.z == mask.idq))) s[c + 2] = -INFINITY;
-        if (!(c + 3 <= lim || (img && id.w == mask.idq))) s[c + 3] = -INFINITY;
-      }
-    } else {
-      // Last tile of the sequence, or ids not 16-byte aligned: one by one.
-      // Keys past n are already masked (valid).
-#pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        const int id = (mask.c0 + c < mask.n) ? __ldg(mask.ids + c) : -1;
-        if (!(c <= lim || (mask.idq >= 0 && id == mask.idq))) s[c] = -INFINITY;
-      }
-    }
-  }
-  if (BC && mask.valid) {
-    if (mask.c0 + BN <= mask.n && (reinterpret_cast<uintptr_t>(mask.valid) & 15u) == 0) {
-      // 128 flags as eight 16-byte loads; the per-key pass (loading them
-      // again) runs only when a flag is zero (zero-byte test per word).
-      const uint4* kv4 = reinterpret_cast<const uint4*>(mask.valid);
-      uint32_t zero = 0;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint4 v = __ldg(kv4 + k);
-        zero |= ((v.x - 0x01010101u) & ~v.x) | ((v.y - 0x01010101u) & ~v.y) |
-                ((v.z - 0x01010101u) & ~v.z) | ((v.w - 0x01010101u) & ~v.w);
-      }
-      if (zero & 0x80808080u) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint4 v = __ldg(kv4 + k);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            if (((w[c / 4] >> (8 * (c % 4))) & 0xffu) == 0) s[16 * k + c] = -INFINITY;
-        }
-      }
-    } else {
-#pragma unroll
-      for (int c = 0; c < BN; ++c)
-        if (mask.c0 + c < mask.n && __ldg(mask.valid + c) == 0) s[c] = -INFINITY;
-    }
+    for (int c = 0; c < BN; ++c)
+      if (!((vis[c / 32] >> (c % 32)) & 1u)) s[c] = -INFINITY;
   }
   // Row maximum: four independent chains of 3-input max.
   float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
@@ -696,7 +727,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int T = T0 + p.n_tiles[1];
   const uint64_t limit = p.wait_limit_ns;
   const int n_items = p.n_items;
-  const int stride = static_cast<int>(gridDim.x);
 
   const uint32_t ring = base_u32 + C::RING_OFF;
   const uint32_t qs = base_u32 + C::Q_OFF;
@@ -790,7 +820,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       int n = 0;  // units done by this CTA
       bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += stride, ++n) {
+      for (int item = item_at<BC>(0); item < n_items && ok; item = item_at<BC>(++n)) {
         const Item it = decode_item<BC>(p, item, T);
         const Unit& u = it.u;
         // The Q buffers are free once every S MMA of the previous item is done.
@@ -874,7 +904,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         issue_pv(i, v_slot, accumulate);
         return true;
       };
-      for (int item = blockIdx.x; item < n_items && ok; item += stride, ++n) {
+      for (int item = item_at<BC>(0); item < n_items && ok; item = item_at<BC>(++n)) {
         const Item it = decode_item<BC>(p, item, T);
         const int nq = it.u.two ? 2 : 1;
         ok = wait_bounded(bar_q, n & 1, limit, abort_flag, 2);
@@ -933,7 +963,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t bar_part = smem_u32(&ctl->part_done[i]);
     const uint32_t bar_merge = smem_u32(&ctl->merge_ready[i]);
     const int row = wq * 32 + lane;  // row of the 128-row query tile (= TMEM lane)
-    for (int item = blockIdx.x; item < n_items && ok; item += stride) {
+    for (int n = 0, item = item_at<BC>(0); item < n_items && ok; item = item_at<BC>(++n)) {
       const Item it = decode_item<BC>(p, item, T);
       const Unit& u = it.u;
       if (i == 1 && !u.two) continue;
