@@ -1,0 +1,840 @@
+// The attention kernel: work items, the per-tile online softmax and the
+// warp-specialised persistent kernel (TMA loader, tcgen05 issuer, softmax /
+// correction / epilogue warps).  Included once, by attn_fwd.cu, which holds
+// the host side and the C ABI.
+#pragma once
+
+#include "sm103_ptx.cuh"
+
+namespace ncp {
+
+constexpr int BM = 128;                  // query rows per tile (one TMEM lane each)
+constexpr int BN = 128;                  // keys per KV tile
+constexpr int NUM_THREADS = 320;
+constexpr int PRODUCER_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr uint32_t TMEM_COLS = 512;
+// TMEM column of S_i and O_i for query tile i.
+__host__ __device__ constexpr uint32_t tmem_s_col(int i) { return 128u * i; }
+__host__ __device__ constexpr uint32_t tmem_o_col(int i) { return 256u + 128u * i; }
+constexpr int MAX_SLOTS = 8;
+// Block-causal form: per-CTA table of the image ids in each 128-token tile
+// (min, max and "one image only"), held in shared memory; N <= 128 * this.
+constexpr int MAX_SEQ_TILES = 1024;
+// Rescale O only when the running row maximum (log2 units) grows by more than
+// this; otherwise keep the stale maximum.  Exact, because the final 1/l uses
+// the same maximum as the accumulated O, and p <= 2^8 stays far from overflow.
+constexpr float RESCALE_THRESHOLD = 8.0f;
+
+// Polynomial share of the exponentials (compile-time; overridable with -D).
+#ifndef NCP_POLY_NUM_D128
+#define NCP_POLY_NUM_D128 0
+#endif
+#ifndef NCP_POLY_DEN_D128
+#define NCP_POLY_DEN_D128 4
+#endif
+#ifndef NCP_POLY_NUM_D64
+#define NCP_POLY_NUM_D64 0
+#endif
+#ifndef NCP_POLY_DEN_D64
+#define NCP_POLY_DEN_D64 4
+#endif
+
+template <int D>
+struct Cfg {
+  static constexpr int CHUNKS = D / 64;                  // 128-byte swizzle columns per row
+  static constexpr uint32_t TILE_BYTES = BN * D * 2;     // one K or V tile; one Q tile (BM == BN)
+  static constexpr uint32_t CHUNK_BYTES = BN * 128;      // 128 rows x 128 bytes
+  static constexpr int NSLOT = (D == 128) ? 4 : 8;       // K/V ring slots
+  static constexpr uint32_t RING_OFF = 0;
+  static constexpr uint32_t Q_OFF = RING_OFF + NSLOT * TILE_BYTES;
+  static constexpr uint32_t BAR_OFF = Q_OFF + 2 * TILE_BYTES;
+  static constexpr uint32_t SMEM_BYTES = BAR_OFF + 512 + 1024;  // barriers + 1 KiB alignment slack
+  static constexpr uint32_t SUM_OFF = BAR_OFF + 512;             // block-causal tile table
+  static constexpr uint32_t SMEM_BYTES_BC = SUM_OFF + 3 * 4 * MAX_SEQ_TILES + 1024;
+  // Share of the exponentials computed by the FMA-pipe polynomial instead of
+  // the MUFU unit: POLY_NUM of every POLY_DEN packed pairs.  On GB300 the
+  // MUFU unit does about 30 exp2 per clock per SM and the polynomial about 13:
+  // every measured share above 0 was slower, so the default is 0.
+  static constexpr int POLY_NUM = (D == 128) ? NCP_POLY_NUM_D128 : NCP_POLY_NUM_D64;
+  static constexpr int POLY_DEN = (D == 128) ? NCP_POLY_DEN_D128 : NCP_POLY_DEN_D64;
+  static_assert(POLY_DEN >= 1 && POLY_NUM >= 0 && POLY_NUM <= POLY_DEN, "polynomial share");
+  __host__ __device__ static constexpr bool poly_pair(int c) { return (c % POLY_DEN) >= POLY_DEN - POLY_NUM; }
+};
+
+struct SharedCtl {
+  uint64_t q_full;
+  uint64_t q_free;
+  uint64_t kv_full[MAX_SLOTS];
+  uint64_t kv_empty[MAX_SLOTS];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_full[2];
+  uint64_t o_free[2];
+  uint64_t part_done[2];   // the 4 warps of a query tile wrote their partial rows
+  uint64_t merge_ready[2]; // the piece's arrival count is known (SharedCtl::last)
+  uint64_t drain;
+  int last[2];             // this piece is the last of its unit: merge and store
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+struct Params {
+  CUtensorMap tm_q;
+  CUtensorMap tm_k[2];   // [0] prefix segment, [1] current segment
+  CUtensorMap tm_v[2];
+  __nv_bfloat16* out;
+  // Masked forms (block-causal, masked prefix-cached): image id per key
+  // position [Np + Nq] (-1 = text) and, optionally, key_valid [B, Np + Nq]
+  // (nullptr: every key valid).  Query i sits at position Np + i.
+  const int* image_ids;
+  const unsigned char* key_valid;
+  int Nq, H;
+  int q_pairs;           // ceil(Nq / 256): units per (b, h); units are (b, h, q pair), q pair fastest
+  // Work items, walked round-robin by the persistent CTAs: items [0, n_whole)
+  // are whole units; the units of the last, partly filled round are cut into
+  // `pieces` key ranges each (items n_whole + r * pieces + k), merged through
+  // the workspace by whichever piece of a unit finishes last.
+  int n_items;
+  int n_whole;
+  int pieces;
+  float* ws_part;          // [split unit][piece][query tile][128 rows][D + 4]: O, m, l
+  unsigned int* ws_count;  // [split unit][query tile] finished pieces (reset by the merger)
+  int n_tok[2];          // tokens per key segment
+  int n_tiles[2];        // KV tiles per key segment
+  float scale_log2;      // D^-0.5 * log2(e)
+  int fault_mode;
+  unsigned long long wait_limit_ns;
+};
+
+// ----------------------------------------------------------------------------
+// Work units and the softmax of one score tile
+// ----------------------------------------------------------------------------
+struct Unit {
+  int b, h, q0;
+  bool two;  // the second 128-row query tile has at least one row
+};
+
+template <bool BC>
+__device__ __forceinline__ Unit decode_unit(const Params& p, int unit) {
+  Unit u;
+  // Dense forms: query pair fastest, so the CTAs running at one time share
+  // the K/V of a few heads in L2.  Masked forms: rows see more keys the later
+  // they sit, so hand out the last query pairs first, over all heads (longest
+  // work first; all heads' K/V stay in L2 at these lengths).
+  const int n_bh = p.H * (p.n_items / (p.q_pairs * p.H));  // B * H (masked forms never split)
+  const int qp = BC ? p.q_pairs - 1 - unit / n_bh : unit % p.q_pairs;
+  const int bh = BC ? unit % n_bh : unit / p.q_pairs;
+  u.h = bh % p.H;
+  u.b = bh / p.H;
+  u.q0 = qp * (2 * BM);
+  u.two = (u.q0 + BM) < p.Nq;
+  return u;
+}
+
+struct Item {
+  Unit u;
+  int t_begin, t_end;  // key tiles [t_begin, t_end) of the concatenated key sequence
+  int split;           // -1: whole unit; else index of the split unit
+  int piece;
+};
+
+// The n-th item of this CTA.  Dense forms: round robin.  Masked forms (units
+// of unequal work, longest first): a snake, so that CTAs that took a long
+// unit in one round take a short one in the next.
+template <bool BC>
+__device__ __forceinline__ int item_at(int n) {
+  const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return n * g + ((BC && (n & 1)) ? g - 1 - c : c);
+}
+
+template <bool BC>
+__device__ __forceinline__ Item decode_item(const Params& p, int item, int T) {
+  Item it;
+  int unit;
+  if (item < p.n_whole) {
+    unit = item;
+    it.split = -1;
+    it.piece = 0;
+    it.t_begin = 0;
+    it.t_end = T;
+  } else {
+    const int r = (item - p.n_whole) / p.pieces;
+    const int k = (item - p.n_whole) % p.pieces;
+    unit = p.n_whole + r;
+    it.split = r;
+    it.piece = k;
+    it.t_begin = (k * T) / p.pieces;
+    it.t_end = ((k + 1) * T) / p.pieces;
+  }
+  it.u = decode_unit<BC>(p, unit);
+  return it;
+}
+
+// Block-causal visibility (definition prefix_cached_block_causal_h32_d128_
+// prefix0): query i sees key j iff j <= i, or both carry the same image id >= 0.
+// Tiles are summarised by the range [lo, hi] of their non-negative ids (lo >
+// hi: text only) and by `uni` (every token in one image).
+struct TileTable {
+  const int* lo;
+  const int* hi;
+  const int* uni;
+};
+
+// Key tiles walk the prefix segment (tiles [0, T0)) then the current one;
+// position of the first key of tile t, and its number of keys.
+__device__ __forceinline__ int key_tile_pos(const Params& p, int t) {
+  const int T0 = p.n_tiles[0];
+  return t < T0 ? t * BN : p.n_tok[0] + (t - T0) * BN;
+}
+__device__ __forceinline__ int key_tile_len(const Params& p, int t) {
+  const int T0 = p.n_tiles[0];
+  const int seg = t < T0 ? 0 : 1;
+  return min(BN, p.n_tok[seg] - (t - (seg ? T0 : 0)) * BN);
+}
+
+// Some query row of the unit sees some key of tile t: causally (the tile
+// starts at or before the unit's last row, at position Np + row), or through
+// an image id both may share (their id ranges meet; the query tiles are the
+// current segment's tiles T0 + qt).  key_valid only removes keys, so the
+// filter stays exact: a skipped tile has no visible pair.
+__device__ __forceinline__ bool bc_unit_visits(const TileTable& tt, const Params& p, const Unit& u,
+                                               int t) {
+  const int r_last = p.n_tok[0] + min(u.q0 + 2 * BM, p.Nq) - 1;
+  if (key_tile_pos(p, t) <= r_last) return true;
+  const int qt0 = p.n_tiles[0] + u.q0 / BM;
+  const int qt1 = u.two ? qt0 + 1 : qt0;
+  const int qlo = min(tt.lo[qt0], tt.lo[qt1]);
+  const int qhi = max(tt.hi[qt0], tt.hi[qt1]);
+  return qlo <= tt.hi[t] && tt.lo[t] <= qhi;
+}
+
+// Every query row of query tile qt (current-segment tile T0 + qt, first row
+// q_first) sees every key of tile t through causality or one shared image
+// (key_valid aside): the keys all precede the rows, or both tiles hold one
+// and the same image.
+__device__ __forceinline__ bool bc_tile_full(const TileTable& tt, const Params& p, int qt,
+                                             int q_first, int t) {
+  if (key_tile_pos(p, t) + key_tile_len(p, t) - 1 <= p.n_tok[0] + q_first) return true;
+  const int tq = p.n_tiles[0] + qt;
+  return tt.uni[tq] && tt.uni[t] && tt.lo[tq] == tt.lo[t];
+}
+
+// Per-row mask of one key tile of the masked forms: key position c0 + c is
+// visible to the query at position qi (image id idq) iff c0 + c <= qi or its
+// id equals idq >= 0, and (with key_valid) the key is valid.
+struct RowMask {
+  const int* ids;  // image ids of the tile's keys (ids[0] is key c0); nullptr: all visible
+  const unsigned char* valid;  // key_valid of the tile's keys for this batch; nullptr: all valid
+  int c0, qi, idq, n;  // n: key positions (Np + Nq; nothing past n is read)
+};
+
+// One 128-key tile of the online softmax for this thread's query row:
+// S (fp32, TMEM) -> running max m and sum l (log2 domain) -> P (bf16) written
+// over the first 64 columns of S; O is rescaled in TMEM when m moved.
+template <int D, bool BC>
+__device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, int valid, float sl2,
+                                             bool may_rescale, const RowMask& mask, float& m,
+                                             float& l) {
+  // Masked forms: this row's visibility of the tile's 128 keys as a bitmask,
+  // built before the scores are loaded so that fewer registers are live.
+  uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
+  bool masked = false;
+  if (BC && mask.ids) {
+    masked = true;
+    const int lim = mask.qi - mask.c0;  // keys c <= lim are visible causally
+    const bool img = mask.idq >= 0;
+    if (mask.c0 + BN <= mask.n && (mask.c0 & 3) == 0) {
+      const int4* ids4 = reinterpret_cast<const int4*>(mask.ids);
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        uint32_t w = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int4 id = __ldg(ids4 + 8 * g + k);
+          const int c = 32 * g + 4 * k;
+          w |= static_cast<uint32_t>(c + 0 <= lim || (img && id.x == mask.idq)) << (4 * k + 0);
+          w |= static_cast<uint32_t>(c + 1 <= lim || (img && id.y == mask.idq)) << (4 * k + 1);
+          w |= static_cast<uint32_t>(c + 2 <= lim || (img && id.z == mask.idq)) << (4 * k + 2);
+          w |= static_cast<uint32_t>(c + 3 <= lim || (img && id.w == mask.idq)) << (4 * k + 3);
+        }
+        vis[g] = w;
+      }
+    } else {
+      // Last tile of the sequence, or ids not 16-byte aligned: one by one.
+      // Keys past n are masked by `valid` below.
+#pragma unroll
+      for (int c = 0; c < BN; ++c) {
+        const int id = (mask.c0 + c < mask.n) ? __ldg(mask.ids + c) : -1;
+        if (!(c <= lim || (img && id == mask.idq))) vis[c / 32] &= ~(1u << (c % 32));
+      }
+    }
+  }
+  if (BC && mask.valid) {
+    if (mask.c0 + BN <= mask.n && (reinterpret_cast<uintptr_t>(mask.valid) & 15u) == 0) {
+      // 128 flags as eight 16-byte loads; the per-key pass runs only when a
+      // flag is zero (zero-byte test per 32-bit word).
+      const uint4* kv4 = reinterpret_cast<const uint4*>(mask.valid);
+      uint32_t zero = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint4 v = __ldg(kv4 + k);
+        zero |= ((v.x - 0x01010101u) & ~v.x) | ((v.y - 0x01010101u) & ~v.y) |
+                ((v.z - 0x01010101u) & ~v.z) | ((v.w - 0x01010101u) & ~v.w);
+      }
+      if (zero & 0x80808080u) {
+        masked = true;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 v = __ldg(kv4 + k);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            if (((w[c / 4] >> (8 * (c % 4))) & 0xffu) == 0)
+              vis[(16 * k + c) / 32] &= ~(1u << ((16 * k + c) % 32));
+        }
+      }
+    } else {
+      masked = true;
+#pragma unroll
+      for (int c = 0; c < BN; ++c)
+        if (mask.c0 + c < mask.n && __ldg(mask.valid + c) == 0) vis[c / 32] &= ~(1u << (c % 32));
+    }
+  }
+  float s[BN];
+  {
+    uint32_t r[BN];
+#pragma unroll
+    for (int c = 0; c < BN; c += 32) tmem_ld32(s_addr + c, r + c);
+    tmem_wait_ld();
+#pragma unroll
+    for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(r[c]);
+  }
+  if (valid < BN) {
+#pragma unroll
+    for (int c = 0; c < BN; ++c)
+      if (c >= valid) s[c] = -INFINITY;
+  }
+  if (BC && masked) {
+#pragma unroll
+    for (int c = 0; c < BN; ++c)
+      if (!((vis[c / 32] >> (c % 32)) & 1u)) s[c] = -INFINITY;
+  }
+  // Row maximum: four independent chains of 3-input max.
+  float mx0 = fmax3(s[0], s[1], s[2]), mx1 = fmax3(s[3], s[4], s[5]);
+  float mx2 = fmax3(s[6], s[7], s[8]), mx3 = fmax3(s[9], s[10], s[11]);
+#pragma unroll
+  for (int c = 12; c + 8 <= BN; c += 8) {
+    mx0 = fmax3(mx0, s[c], s[c + 1]);
+    mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+    mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+    mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
+  }
+  mx0 = fmax3(mx0, s[BN - 4], s[BN - 3]);
+  mx1 = fmax3(mx1, s[BN - 2], s[BN - 1]);
+  const float m_tile = fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
+  float alpha = 1.f;
+  bool rescale = false;
+  if (m_tile > m + RESCALE_THRESHOLD) {
+    alpha = ex2(m - m_tile);
+    l *= alpha;
+    m = m_tile;
+    rescale = may_rescale;
+  }
+  // p = 2^(s * scale * log2(e) - m) on packed pairs; pairs selected by
+  // poly_pair go through the FMA-pipe polynomial, the rest through MUFU.
+  const uint64_t sl2x2 = pk2(sl2, sl2);
+  // A row with no visible key yet (block-causal form only) keeps m = -inf:
+  // use 0 so that its masked scores give p = 0 instead of NaN.
+  const float m_ref = (BC && m == -INFINITY) ? 0.f : m;
+  const uint64_t neg_m2 = pk2(-m_ref, -m_ref);
+  uint64_t acc0 = 0, acc1 = 0;  // two packed running sums (bits 0 = 0.0f)
+  uint32_t pk[BN / 2];
+#pragma unroll
+  for (int c = 0; c < BN / 2; ++c) {
+    const uint64_t x = ffma2(pk2(s[2 * c], s[2 * c + 1]), sl2x2, neg_m2);
+    float p0, p1;
+    if (Cfg<D>::poly_pair(c)) {
+      exp2_poly2(x, p0, p1);
+    } else {
+      float x0, x1;
+      up2(x, x0, x1);
+      p0 = ex2(x0);
+      p1 = ex2(x1);
+    }
+    if (c & 1)
+      acc1 = fadd2(acc1, pk2(p0, p1));
+    else
+      acc0 = fadd2(acc0, pk2(p0, p1));
+    pk[c] = pack_bf16x2(p0, p1);
+  }
+  {
+    float a0, a1, a2, a3;
+    up2(acc0, a0, a1);
+    up2(acc1, a2, a3);
+    l += (a0 + a1) + (a2 + a3);
+  }
+  tmem_st32(s_addr + 0, pk);
+  tmem_st32(s_addr + 32, pk + 32);
+  if (__any_sync(0xffffffffu, rescale)) {
+    // O holds the complete sum through the previous tile: this S was issued
+    // after the previous P V and its commit has fired.  Rows of this warp
+    // that keep their maximum scale by 1.
+    const uint64_t alpha2 = pk2(alpha, alpha);
+#pragma unroll
+    for (int c = 0; c < D; c += 32) {
+      uint32_t r[32];
+      tmem_ld32(o_addr + c, r);
+      tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 32; e += 2) {
+        float a0, a1;
+        up2(fmul2(pk2(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), alpha2), a0, a1);
+        r[e] = __float_as_uint(a0);
+        r[e + 1] = __float_as_uint(a1);
+      }
+      tmem_st32(o_addr + c, r);
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------
+// The kernel
+// ----------------------------------------------------------------------------
+// BC = false: dense and prefix-cached forms (every key visible).
+// BC = true: block-causal form (one key segment, per-row image-id mask).
+template <int D, bool BC>
+// 10 warps on 4 SM sub-partitions (16 Ki registers each, 3 warps on two of
+// them) cap a thread at 168 registers.
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ Params p) {
+  using C = Cfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment for the 128-byte swizzle atoms.
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base_u32 = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* base = smem_raw + (base_u32 - raw_u32);
+  SharedCtl* ctl = reinterpret_cast<SharedCtl*>(base + C::BAR_OFF);
+  volatile int* abort_flag = &ctl->abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int T0 = p.n_tiles[0];
+  const int T = T0 + p.n_tiles[1];
+  const uint64_t limit = p.wait_limit_ns;
+  const int n_items = p.n_items;
+
+  const uint32_t ring = base_u32 + C::RING_OFF;
+  const uint32_t qs = base_u32 + C::Q_OFF;
+  const uint32_t bar_q = smem_u32(&ctl->q_full);
+  const uint32_t bar_qfree = smem_u32(&ctl->q_free);
+  auto bar_kv_full = [&](int s) { return smem_u32(&ctl->kv_full[s]); };
+  auto bar_kv_empty = [&](int s) { return smem_u32(&ctl->kv_empty[s]); };
+  const uint32_t bar_s[2] = {smem_u32(&ctl->s_full[0]), smem_u32(&ctl->s_full[1])};
+  const uint32_t bar_p[2] = {smem_u32(&ctl->p_full[0]), smem_u32(&ctl->p_full[1])};
+  const uint32_t bar_o[2] = {smem_u32(&ctl->o_full[0]), smem_u32(&ctl->o_full[1])};
+  const uint32_t bar_ofree[2] = {smem_u32(&ctl->o_free[0]), smem_u32(&ctl->o_free[1])};
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q, 1);
+    mbar_init(bar_qfree, 1);
+    for (int s = 0; s < C::NSLOT; ++s) {
+      mbar_init(bar_kv_full(s), 1);
+      mbar_init(bar_kv_empty(s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_s[i], 1);
+      mbar_init(bar_p[i], 4);      // one arrival per softmax warp
+      mbar_init(bar_o[i], 1);
+      mbar_init(bar_ofree[i], 4);  // one arrival per softmax warp
+      mbar_init(smem_u32(&ctl->part_done[i]), 4);
+      mbar_init(smem_u32(&ctl->merge_ready[i]), 1);
+    }
+    mbar_init(smem_u32(&ctl->drain), 1);
+    ctl->abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == MMA_WARP) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&ctl->tmem_base)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // Masked forms: summarise the image ids of every key tile.
+  const int n_all = p.n_tok[0] + p.n_tok[1];
+  TileTable tt{nullptr, nullptr, nullptr};
+  if constexpr (BC) {
+    int* t_lo = reinterpret_cast<int*>(base + C::SUM_OFF);
+    int* t_hi = t_lo + MAX_SEQ_TILES;
+    int* t_uni = t_hi + MAX_SEQ_TILES;
+    for (int t = warp; t < T; t += NUM_THREADS / 32) {
+      int lo = 0x7fffffff, hi = -1;
+      bool text = false;
+      const int pos0 = key_tile_pos(p, t), len = key_tile_len(p, t);
+      for (int e = lane; e < BN; e += 32) {
+        const int j = pos0 + e;
+        if (e < len) {
+          const int id = __ldg(p.image_ids + j);
+          if (id < 0) {
+            text = true;
+          } else {
+            lo = min(lo, id);
+            hi = max(hi, id);
+          }
+        }
+      }
+      lo = __reduce_min_sync(0xffffffffu, lo);
+      hi = __reduce_max_sync(0xffffffffu, hi);
+      text = __any_sync(0xffffffffu, text);
+      if (lane == 0) {
+        t_lo[t] = lo;
+        t_hi[t] = hi;
+        t_uni[t] = (!text && lo == hi) ? 1 : 0;
+      }
+    }
+    tt = TileTable{t_lo, t_hi, t_uni};
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  // Loader bookkeeping for draining copies in flight after an abort.
+  uint32_t ld_issued = 0, ld_parity = 0;  // per ring slot: a load was issued / its phase
+  int q_last = -1;                        // last unit whose Q load was issued
+
+  if (warp == PRODUCER_WARP) {
+    // ---------------------------------------------------------------- loader
+    if (lane == 0) {
+      prefetch_tmap(&p.tm_q);
+      for (int s = 0; s < 2; ++s) {
+        prefetch_tmap(&p.tm_k[s]);
+        prefetch_tmap(&p.tm_v[s]);
+      }
+      int slot = 0;
+      uint32_t phase = 0;
+      int n = 0;  // units done by this CTA
+      bool ok = true;
+      for (int item = item_at<BC>(0); item < n_items && ok; item = item_at<BC>(++n)) {
+        const Item it = decode_item<BC>(p, item, T);
+        const Unit& u = it.u;
+        // The Q buffers are free once every S MMA of the previous item is done.
+        if (n > 0) {
+          ok = wait_bounded(bar_qfree, (n - 1) & 1, limit, abort_flag, 9);
+          if (!ok) break;
+        }
+        const int nq_tiles = u.two ? 2 : 1;
+        mbar_expect_tx(bar_q, nq_tiles * C::TILE_BYTES);
+        for (int i = 0; i < nq_tiles; ++i)
+          for (int c = 0; c < C::CHUNKS; ++c)
+            tma_load_4d(qs + i * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tm_q, c * 64, u.h,
+                        u.q0 + i * BM, u.b, bar_q);
+        q_last = n;
+        for (int t = it.t_begin; t < it.t_end && ok; ++t) {
+          if (BC && !bc_unit_visits(tt, p, u, t)) continue;
+          const int seg = (t < T0) ? 0 : 1;
+          const int tok0 = (t - (seg ? T0 : 0)) * BN;
+          for (int kind = 0; kind < 2; ++kind) {
+            ok = wait_bounded(bar_kv_empty(slot), phase ^ 1u, limit, abort_flag, 1);
+            if (!ok) break;
+            const bool skip = (p.fault_mode == 1) && kind == 1 && t == 1 && item == 0;
+            if (!skip) {
+              const CUtensorMap* map = kind == 0 ? &p.tm_k[seg] : &p.tm_v[seg];
+              mbar_expect_tx(bar_kv_full(slot), C::TILE_BYTES);
+              for (int c = 0; c < C::CHUNKS; ++c)
+                tma_load_4d(ring + slot * C::TILE_BYTES + c * C::CHUNK_BYTES, map, c * 64, u.h,
+                            tok0, u.b, bar_kv_full(slot));
+              ld_issued |= 1u << slot;
+              ld_parity = (ld_parity & ~(1u << slot)) | (phase << slot);
+            }
+            if (++slot == C::NSLOT) {
+              slot = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = make_idesc(BM, BN, false);
+      constexpr uint32_t IDESC_PV = make_idesc(BM, D, true);
+      // S_i = Q_i K^T over D in K-steps of 16 (32 bytes inside a 128-byte row).
+      auto issue_s = [&](int i, int k_slot) {
+        const uint32_t qa = qs + i * C::TILE_BYTES;
+        const uint32_t kb = ring + k_slot * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+          mma_ss(tmem + tmem_s_col(i), sw128_desc(qa + off, 16, 1024),
+                 sw128_desc(kb + off, 16, 1024), IDESC_S, kk > 0);
+        }
+      };
+      // O_i += P_i V over the BN keys in K-steps of 16 rows of V (MN-major B).
+      auto issue_pv = [&](int i, int v_slot, bool accumulate) {
+        const uint32_t vb = ring + v_slot * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(tmem + tmem_o_col(i), tmem + tmem_s_col(i) + kk * 8,
+                 sw128_desc(vb + kk * 16 * 128, C::CHUNK_BYTES, 1024), IDESC_PV,
+                 (accumulate || kk > 0) ? 1u : 0u);
+      };
+
+      int slot = 0;
+      uint32_t phase = 0;
+      uint32_t sc[2] = {0u, 0u};  // S commits per query tile (phases of s_full / p_full)
+      uint32_t oc[2] = {0u, 0u};  // units finished per query tile (phases of o_full / o_free)
+      bool ok = true;
+      int n = 0;
+      // The first P V of a unit overwrites O_i: wait until the epilogue of the
+      // previous unit has read it out of TMEM.
+      auto pv = [&](int i, int v_slot, bool accumulate) -> bool {
+        if (!wait_bounded(bar_p[i], (sc[i] - 1u) & 1u, limit, abort_flag, 4)) return false;
+        if (!accumulate && oc[i] > 0 &&
+            !wait_bounded(bar_ofree[i], (oc[i] - 1u) & 1u, limit, abort_flag, 6))
+          return false;
+        tc_fence_after();
+        issue_pv(i, v_slot, accumulate);
+        return true;
+      };
+      for (int item = item_at<BC>(0); item < n_items && ok; item = item_at<BC>(++n)) {
+        const Item it = decode_item<BC>(p, item, T);
+        const int nq = it.u.two ? 2 : 1;
+        ok = wait_bounded(bar_q, n & 1, limit, abort_flag, 2);
+        if (!ok) break;
+        int v_prev = -1;
+        int j = 0;  // key tiles visited so far in this item
+        for (int t = it.t_begin; t < it.t_end && ok; ++t) {
+          if (BC && !bc_unit_visits(tt, p, it.u, t)) continue;
+          const int k_slot = slot;
+          ok = wait_bounded(bar_kv_full(k_slot), phase, limit, abort_flag, 3);
+          if (!ok) break;
+          if (++slot == C::NSLOT) { slot = 0; phase ^= 1u; }
+          tc_fence_after();
+          for (int i = 0; i < nq && ok; ++i) {
+            if (j > 0) {
+              ok = pv(i, v_prev, j - 1 > 0);
+              if (!ok) break;
+            }
+            issue_s(i, k_slot);
+            mma_commit(bar_s[i]);
+            ++sc[i];
+          }
+          if (!ok) break;
+          if (j > 0) mma_commit(bar_kv_empty(v_prev));
+          mma_commit(bar_kv_empty(k_slot));
+          const int v_slot = slot;
+          ok = wait_bounded(bar_kv_full(v_slot), phase, limit, abort_flag, 5);
+          if (!ok) break;
+          if (++slot == C::NSLOT) { slot = 0; phase ^= 1u; }
+          v_prev = v_slot;
+          ++j;
+        }
+        if (!ok) break;
+        mma_commit(bar_qfree);  // every S MMA of this item has been issued
+        for (int i = 0; i < nq && ok; ++i) {
+          ok = pv(i, v_prev, j - 1 > 0);
+          if (!ok) break;
+          mma_commit(bar_o[i]);
+          ++oc[i];
+        }
+        if (ok) mma_commit(bar_kv_empty(v_prev));
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------- softmax / correction / store
+    const int i = warp >> 2;  // query tile
+    const int wq = warp & 3;  // TMEM lane quarter
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t s_addr = tmem + lane_base + tmem_s_col(i);
+    const uint32_t o_addr = tmem + lane_base + tmem_o_col(i);
+    const float sl2 = p.scale_log2;
+    uint32_t sc = 0, oc = 0;  // phases of s_full / p_full and of o_full / o_free
+    bool ok = true;
+    uint32_t mc = 0;  // split items done by this query tile (phases of part_done / merge_ready)
+    const uint32_t bar_part = smem_u32(&ctl->part_done[i]);
+    const uint32_t bar_merge = smem_u32(&ctl->merge_ready[i]);
+    const int row = wq * 32 + lane;  // row of the 128-row query tile (= TMEM lane)
+    for (int n = 0, item = item_at<BC>(0); item < n_items && ok; item = item_at<BC>(++n)) {
+      const Item it = decode_item<BC>(p, item, T);
+      const Unit& u = it.u;
+      if (i == 1 && !u.two) continue;
+      float m = -INFINITY;  // running (possibly stale) maximum, log2 units
+      float l = 0.f;        // running sum of exp2(x - m)
+      RowMask mask{nullptr, nullptr, 0, 0, -1, n_all};
+      if constexpr (BC) {
+        const int qrow = u.q0 + i * BM + row;  // query index; past Nq: a padding row
+        mask.qi = p.n_tok[0] + qrow;
+        mask.idq = qrow < p.Nq ? __ldg(p.image_ids + mask.qi) : -1;
+      }
+      int j = 0;  // key tiles visited so far in this item
+      for (int t = it.t_begin; t < it.t_end; ++t) {
+        if constexpr (BC) {
+          if (!bc_unit_visits(tt, p, u, t)) continue;
+          const bool full = bc_tile_full(tt, p, u.q0 / BM + i, u.q0 + i * BM, t);
+          mask.c0 = key_tile_pos(p, t);
+          mask.ids = full ? nullptr : p.image_ids + mask.c0;
+          mask.valid = p.key_valid ? p.key_valid + static_cast<size_t>(u.b) * n_all + mask.c0
+                                   : nullptr;
+        }
+        ok = warp_wait(bar_s[i], sc & 1u, limit, abort_flag, 7);
+        if (!ok) break;
+        ++sc;
+        tc_fence_after();
+        // Keys past the end of this segment: TMA filled them with zeros, their
+        // scores must be -inf instead.
+        const int seg = (t < T0) ? 0 : 1;
+        const int valid = p.n_tok[seg] - (t - (seg ? T0 : 0)) * BN;
+        softmax_tile<D, BC>(s_addr, o_addr, valid, sl2, j > 0, mask, m, l);
+        ++j;
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_p[i]);
+      }
+      if (!ok) break;
+      ok = warp_wait(bar_o[i], oc & 1u, limit, abort_flag, 8);
+      if (!ok) break;
+      ++oc;
+      tc_fence_after();
+      // Epilogue: read O_i out of TMEM and release it to the next item's P V.
+      uint32_t r[D];
+#pragma unroll
+      for (int c = 0; c < D; c += 32) tmem_ld32(o_addr + c, r + c);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_ofree[i]);
+
+      if (it.split >= 0) {
+        // A piece of a split unit: publish (O, m, l) of this row, count the
+        // piece in; the last piece of the unit merges every piece.
+        constexpr int RS = D + 4;  // row stride in floats (16-byte aligned)
+        const size_t tile_rows = static_cast<size_t>(2) * BM;
+        float* part_base = p.ws_part + static_cast<size_t>(it.split) * p.pieces * tile_rows * RS;
+        auto part_row = [&](int k) {
+          return part_base + ((static_cast<size_t>(k) * 2 + i) * BM + row) * RS;
+        };
+        {
+          float4* dst = reinterpret_cast<float4*>(part_row(it.piece));
+#pragma unroll
+          for (int c = 0; c < D; c += 4)
+            __stcg(dst + c / 4, make_float4(__uint_as_float(r[c]), __uint_as_float(r[c + 1]),
+                                            __uint_as_float(r[c + 2]), __uint_as_float(r[c + 3])));
+          __stcg(dst + D / 4, make_float4(m, l, 0.f, 0.f));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_part);
+        if (wq == 0 && lane == 0) {
+          ok = wait_bounded(bar_part, mc & 1u, limit, abort_flag, 10);
+          if (ok) {
+            __threadfence();
+            const unsigned int before = atomicAdd(p.ws_count + it.split * 2 + i, 1u);
+            const int last = before == static_cast<unsigned int>(p.pieces - 1);
+            if (last) {
+              __threadfence();
+              atomicExch(p.ws_count + it.split * 2 + i, 0u);  // ready for the next launch
+            }
+            ctl->last[i] = last;
+            mbar_arrive(bar_merge);
+          }
+        }
+        ok = warp_wait(bar_merge, mc & 1u, limit, abort_flag, 11);
+        ++mc;
+        if (!ok) break;
+        if (!*reinterpret_cast<volatile int*>(&ctl->last[i])) continue;
+        // Merge every piece (this one's included, read back) in piece order,
+        // so the result does not depend on which piece finished last.
+        float m_all = -INFINITY;
+        for (int k = 0; k < p.pieces; ++k) m_all = fmaxf(m_all, __ldcg(part_row(k) + D));
+        l = 0.f;
+#pragma unroll
+        for (int c = 0; c < D; ++c) r[c] = 0u;
+        for (int k = 0; k < p.pieces; ++k) {
+          const float4* src4 = reinterpret_cast<const float4*>(part_row(k));
+          const float4 ml = __ldcg(src4 + D / 4);
+          const float a = ex2(ml.x - m_all);
+          l = fmaf(ml.y, a, l);
+#pragma unroll
+          for (int c = 0; c < D; c += 4) {
+            const float4 v = __ldcg(src4 + c / 4);
+            r[c] = __float_as_uint(fmaf(v.x, a, __uint_as_float(r[c])));
+            r[c + 1] = __float_as_uint(fmaf(v.y, a, __uint_as_float(r[c + 1])));
+            r[c + 2] = __float_as_uint(fmaf(v.z, a, __uint_as_float(r[c + 2])));
+            r[c + 3] = __float_as_uint(fmaf(v.w, a, __uint_as_float(r[c + 3])));
+          }
+        }
+      }
+
+      // O / l -> bf16 -> this thread's output row.
+      const int q = u.q0 + i * BM + row;
+      if (q < p.Nq) {
+        const float inv_l = 1.f / l;
+        const uint64_t inv2 = pk2(inv_l, inv_l);
+        uint4* dst = reinterpret_cast<uint4*>(
+            p.out + ((static_cast<size_t>(u.b) * p.Nq + q) * p.H + u.h) * D);
+#pragma unroll
+        for (int c = 0; c < D; c += 8) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float a0, a1;
+            up2(fmul2(pk2(__uint_as_float(r[c + 2 * e]), __uint_as_float(r[c + 2 * e + 1])), inv2),
+                a0, a1);
+            w[e] = pack_bf16x2(a0, a1);
+          }
+          dst[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // Some role gave up: before the CTA exits and TMEM is released, let every
+    // TMA copy and every MMA still in flight land (bounded waits again).
+    if (warp == PRODUCER_WARP && lane == 0) {
+      if (q_last >= 0) wait_drain(bar_q, q_last & 1, limit);
+      for (int s = 0; s < C::NSLOT; ++s)
+        if (ld_issued & (1u << s)) wait_drain(bar_kv_full(s), (ld_parity >> s) & 1u, limit);
+    }
+    if (warp == MMA_WARP && lane == 0) {
+      mma_commit(smem_u32(&ctl->drain));
+      wait_drain(smem_u32(&ctl->drain), 0, limit);
+    }
+    __syncwarp();
+  }
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// Test probe of the two exp2 paths the softmax uses: mode 0 the FMA-pipe
+// polynomial, mode 1 the MUFU ex2.approx.  One thread per pair of elements.
+__global__ void exp2_probe_kernel(const float* __restrict__ x, float* __restrict__ y, long long n,
+                                  int mode) {
+  const long long k = 2 * (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x);
+  if (k >= n) return;
+  const bool pair = k + 1 < n;
+  const float a = x[k];
+  const float b = pair ? x[k + 1] : 0.f;
+  float y0, y1;
+  if (mode == 0) {
+    exp2_poly2(pk2(a, b), y0, y1);
+  } else {
+    y0 = ex2(a);
+    y1 = ex2(b);
+  }
+  y[k] = y0;
+  if (pair) y[k + 1] = y1;
+}
+
+}  // namespace ncp

@@ -109,6 +109,6 @@ def test_product_path_does_not_import_the_oracle():
     pkg = os.path.dirname(ncp.__file__)
     for root, _, files in os.walk(pkg):
         for f in files:
-            if f.endswith((".py", ".cu", ".h", ".cpp")):
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(root, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f

@@ -21,7 +21,7 @@ BOUND = 1.02e-4
 
 
 def source_coeffs():
-    text = open(os.path.join(CSRC, "attn_fwd.cu")).read()
+    text = open(os.path.join(CSRC, "sm103_ptx.cuh")).read()
     out = []
     for name in ("EXP2_C1", "EXP2_C2", "EXP2_C3"):
         m = re.search(name + r"\s*=\s*(0x[0-9a-fA-Fp.+-]+)f;", text)
