@@ -190,6 +190,25 @@ int attn_debug_set_fault(int mode, unsigned int wait_limit_us);
  */
 int attn_debug_exp2(const float *x, float *y, long long n, int mode, cudaStream_t stream);
 
+/*
+ * Test hook: the work schedule of a dense-family launch (masked = 0: dense,
+ * cross, prefix-cached; masked = 1: block-causal and masked prefix forms),
+ * computed on the host without a GPU.  A launch over B batches, Nq queries,
+ * H heads and n_key_tiles key tiles of 128 on a GPU with `sms` SMs runs
+ * *grid_out persistent CTAs; each item of each CTA is one row of 12 ints:
+ *   cta, n (the CTA's n-th item), b, h, q0 (first query row of the unit's
+ *   pair of 128-row tiles), two (the second tile has rows), t_begin, t_end
+ *   (key tiles [t_begin, t_end)), tail (-1: a whole unit, else its tail
+ *   unit), piece, pieces (this piece's index and the tail unit's piece
+ *   count), slot0 (workspace slot of the tail unit's piece 0).
+ * Rows go to `rows` (caller-owned host memory, cap rows of 12 ints);
+ * *n_rows receives the item count, *slots_out the workspace slots used.
+ * Returns ATTN_OK, ATTN_ERR_NULL, or ATTN_ERR_SHAPE (a size < 1, or more
+ * than cap items: then only cap rows are written).
+ */
+int attn_debug_schedule(int B, int Nq, int H, int n_key_tiles, int sms, int masked, int *rows,
+                        int cap, int *n_rows, int *grid_out, int *slots_out);
+
 #ifdef __cplusplus
 }
 #endif

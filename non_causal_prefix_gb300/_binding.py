@@ -30,6 +30,7 @@ SIGNATURES = {
     "attn_device_status": (_I, [_VP, _UIP]),
     "attn_debug_set_fault": (_I, [_I, ctypes.c_uint]),
     "attn_debug_exp2": (_I, [_VP, _VP, ctypes.c_longlong, _I, _VP]),
+    "attn_debug_schedule": (_I, [_I, _I, _I, _I, _I, _I, _VP, _I, _VP, _VP, _VP]),
     "attn_dense_fwd_noalloc": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
     "attn_block_causal_fwd": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
     "attn_dense_cross_fwd": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _VP]),
@@ -266,3 +267,21 @@ def debug_exp2(x, mode: int, stream=None):
 def debug_set_fault(mode: int, wait_limit_us: int = 0) -> None:
     _check(load_library().attn_debug_set_fault(int(mode), int(wait_limit_us)),
            "attn_debug_set_fault")
+
+
+def debug_schedule(B: int, Nq: int, H: int, n_key_tiles: int, sms: int, masked: bool = False):
+    """The launch schedule for these sizes on a GPU with `sms` SMs, computed on
+    the host: (rows, grid, slots) with rows an int32 array [items, 12] of
+    (cta, n, b, h, q0, two, t_begin, t_end, tail, piece, pieces, slot0)."""
+    import numpy as np
+    lib = load_library()
+    n_rows, grid, slots = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    args = (int(B), int(Nq), int(H), int(n_key_tiles), int(sms), 1 if masked else 0)
+    rc = lib.attn_debug_schedule(*args, None, 0, ctypes.byref(n_rows), ctypes.byref(grid),
+                                 ctypes.byref(slots))
+    if rc not in (0, -2) or (rc == -2 and n_rows.value == 0):
+        _check(rc, "attn_debug_schedule")
+    rows = np.zeros((max(n_rows.value, 1), 12), dtype=np.int32)
+    _check(lib.attn_debug_schedule(*args, rows.ctypes.data, rows.shape[0], ctypes.byref(n_rows),
+                                   ctypes.byref(grid), ctypes.byref(slots)), "attn_debug_schedule")
+    return rows[:n_rows.value], grid.value, slots.value

@@ -30,18 +30,18 @@
 
 // ============================================================================
 // Fixed scratch for attn_dense_fwd_noalloc: the split workspace (arrival
-// counters, then partial rows) of a call that may not allocate, as one static
+// counters, then partials) of a call that may not allocate, as one static
 // device array.  Every GPU that loads this library holds it until the process
-// exits.  Sized for 160 pieces, one per SM of a GPU with up to 160 SMs, at
-// D <= 128: 256-byte aligned counter block, then 160 x 2 x 128 rows x
-// (128 + 4) floats.
+// exits.  Sized for any GPU with up to 160 SMs at D <= 128: 320 counters in a
+// 256-byte aligned block, then 320 partial slots of 2 x 128 x (128 + 4) floats.
 // ============================================================================
 namespace ncp {
-constexpr int NOALLOC_PIECES = 160;
-constexpr size_t NOALLOC_COUNT_BYTES = 2 * NOALLOC_PIECES * sizeof(unsigned int);  // 1280
+constexpr int NOALLOC_SLOTS = 320;
+constexpr int NOALLOC_COUNTERS = 320;
+constexpr size_t NOALLOC_COUNT_BYTES = NOALLOC_COUNTERS * sizeof(unsigned int);  // 1280
 constexpr size_t NOALLOC_PART_BYTES =
-    static_cast<size_t>(NOALLOC_PIECES) * 2 * BM * (128 + 4) * sizeof(float);
-constexpr size_t NOALLOC_SCRATCH_BYTES = NOALLOC_COUNT_BYTES + NOALLOC_PART_BYTES;  // 21.6 MB
+    static_cast<size_t>(NOALLOC_SLOTS) * 2 * (128 + 4) * BM * sizeof(float);
+constexpr size_t NOALLOC_SCRATCH_BYTES = NOALLOC_COUNT_BYTES + NOALLOC_PART_BYTES;  // 43.3 MB
 static_assert(NOALLOC_COUNT_BYTES % 256 == 0, "partial rows start 256-byte aligned");
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 }  // namespace ncp
@@ -101,17 +101,58 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
 // ---------------------------------------------------------------------------
-// Split workspace: partial (O, m, l) rows of the pieces of split units plus one
-// arrival counter per (split unit, query tile).  One per (device, stream), so
-// calls that run concurrently on different streams never share one; created on
-// the first call that splits (cudaMalloc, then a zeroing memset on that
-// stream) and kept until the process exits.
+// Work schedule (see ncp::schedule_item): whole units fill complete rounds of
+// one persistent CTA per SM.  When the units left for a last, partly filled
+// round would leave SMs idle, their key tiles are shared out evenly over the
+// CTAs instead, each unit's pieces merged through a workspace.
 // ---------------------------------------------------------------------------
+// Most pieces one unit's merge reads (plus one for a range boundary).
 constexpr int MAX_PIECES = 8;
-// A piece pays a Q load, a pipeline fill and a partial write + merge: give it
-// at least this many key tiles.
+// A piece pays a Q load, a pipeline fill and a partial write + merge: give
+// each tail CTA at least this many key tiles.
 constexpr int MIN_PIECE_TILES = 4;
 
+// Schedule of n_units units of T key tiles each on `sms` SMs; `can_split`
+// false (masked forms, whose units visit a data-dependent subset of the key
+// tiles, or no workspace) keeps every unit whole.  Returns the grid size.
+int make_sched(ncp::Sched& s, long long n_units, int T, int sms, bool can_split) {
+  s.n_units = static_cast<int>(n_units);
+  s.n_whole = s.n_units;
+  s.tail_units = 0;
+  s.tail_ctas = 0;
+  const long long rem = n_units % sms;
+  if (can_split && rem > 0) {
+    const long long W = rem * T;
+    long long g_tail = sms;
+    if (g_tail > W / MIN_PIECE_TILES) g_tail = W / MIN_PIECE_TILES;
+    if (g_tail > rem * MAX_PIECES) g_tail = rem * MAX_PIECES;
+    if (g_tail > rem) {
+      s.n_whole = static_cast<int>(n_units - rem);
+      s.tail_units = static_cast<int>(rem);
+      s.tail_ctas = static_cast<int>(g_tail);
+      return s.n_whole > 0 ? sms : s.tail_ctas;
+    }
+  }
+  return n_units < sms ? static_cast<int>(n_units) : sms;
+}
+
+// Workspace slots a schedule uses: tail piece (CTA c, tail unit r) takes slot
+// c + r, so fewer than tail_ctas + tail_units.
+int sched_slots(const ncp::Sched& s) { return s.tail_ctas ? s.tail_ctas + s.tail_units - 1 : 0; }
+
+// Bytes of partials for `slots` pieces: 2 query tiles x 128 rows x (128 + 4)
+// floats (O, then m and l, at D <= 128).
+size_t part_bytes(long long slots) {
+  return static_cast<size_t>(slots) * 2 * (128 + 4) * ncp::BM * sizeof(float);
+}
+
+// ---------------------------------------------------------------------------
+// Split workspace: partials of the tail pieces (at most 2 x SMs slots) plus
+// one arrival counter per (tail unit, query tile).  One per (device, stream),
+// so calls that run concurrently on different streams never share one;
+// created on the first call that splits (cudaMalloc, then a zeroing memset on
+// that stream) and kept until the process exits.
+// ---------------------------------------------------------------------------
 struct Workspace {
   float* part = nullptr;
   unsigned int* count = nullptr;
@@ -119,11 +160,6 @@ struct Workspace {
 
 std::mutex g_ws_mutex;
 std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
-
-// Piece slots = SM count (a split schedule never has more pieces than CTAs).
-size_t ws_part_bytes(int sms) {
-  return static_cast<size_t>(sms) * 2 * ncp::BM * (128 + 4) * sizeof(float);
-}
 
 const Workspace* get_workspace(int dev, int sms, cudaStream_t stream) {
   std::lock_guard<std::mutex> lock(g_ws_mutex);
@@ -139,7 +175,7 @@ const Workspace* get_workspace(int dev, int sms, cudaStream_t stream) {
   }
   Workspace ws;
   const size_t count_bytes = static_cast<size_t>(2) * sms * sizeof(unsigned int);
-  if (cudaMalloc(reinterpret_cast<void**>(&ws.part), ws_part_bytes(sms)) != cudaSuccess) {
+  if (cudaMalloc(reinterpret_cast<void**>(&ws.part), part_bytes(2LL * sms)) != cudaSuccess) {
     cudaGetLastError();
     return nullptr;
   }
@@ -153,8 +189,10 @@ const Workspace* get_workspace(int dev, int sms, cudaStream_t stream) {
   return &(g_ws[key] = ws);
 }
 
+// SM count of the current device, with the kernel's shared-memory limit set
+// there (once per device and instantiation).
 template <int D, bool BC>
-int launch(Params& prm, long long n_units, cudaStream_t stream) {
+int configure(int* dev_out, int* sms_out) {
   using C = ncp::Cfg<D>;
   constexpr uint32_t smem = BC ? C::SMEM_BYTES_BC : C::SMEM_BYTES;
   int dev = 0;
@@ -170,33 +208,26 @@ int launch(Params& prm, long long n_units, cudaStream_t stream) {
       return ATTN_ERR_CUDA;
     sm_count[dev] = sms;
   }
-  const int sms = sm_count[dev];
-  // Schedule.  Whole units fill complete rounds of `sms` persistent CTAs; the
-  // units of the last, partly filled round are cut into `pieces` key ranges
-  // each so that round keeps (nearly) every SM busy.
+  *dev_out = dev;
+  *sms_out = sm_count[dev];
+  return ATTN_OK;
+}
+
+template <int D, bool BC>
+int launch(Params& prm, long long n_units, cudaStream_t stream) {
+  using C = ncp::Cfg<D>;
+  constexpr uint32_t smem = BC ? C::SMEM_BYTES_BC : C::SMEM_BYTES;
+  int dev = 0, sms = 0;
+  if (configure<D, BC>(&dev, &sms) != ATTN_OK) return ATTN_ERR_CUDA;
   const int T = prm.n_tiles[0] + prm.n_tiles[1];
-  const long long rem = n_units % sms;
-  long long pieces = 1;
-  // The block-causal form visits a data-dependent subset of the key tiles, so
-  // a fixed key range could hold none of them: its units are never split.
-  if (rem > 0 && !BC) {
-    pieces = sms / rem;
-    if (pieces > T / MIN_PIECE_TILES) pieces = T / MIN_PIECE_TILES;
-    if (pieces > MAX_PIECES) pieces = MAX_PIECES;
+  int grid = make_sched(prm.sc, n_units, T, sms, !BC);
+  const Workspace* ws = nullptr;
+  if (prm.sc.tail_ctas > 0) {
+    ws = get_workspace(dev, sms, stream);
+    if (!ws) grid = make_sched(prm.sc, n_units, T, sms, false);
   }
-  const Workspace* ws = pieces >= 2 ? get_workspace(dev, sms, stream) : nullptr;
-  if (!ws) pieces = 1;
-  const long long n_whole = pieces >= 2 ? n_units - rem : n_units;
-  const long long n_items = n_whole + (n_units - n_whole) * pieces;
-  if (n_items > 0x7fffffffLL) return ATTN_ERR_SHAPE;
-  prm.n_whole = static_cast<int>(n_whole);
-  prm.n_items = static_cast<int>(n_items);
-  prm.pieces = static_cast<int>(pieces);
   prm.ws_part = ws ? ws->part : nullptr;
   prm.ws_count = ws ? ws->count : nullptr;
-  // Persistent grid: one CTA per SM (shared memory and TMEM allow one), each
-  // walking the items round-robin.
-  const int grid = n_items < sms ? static_cast<int>(n_items) : sms;
   ncp::attn_fwd_kernel<D, BC><<<grid, ncp::NUM_THREADS, smem, stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -239,7 +270,10 @@ int prepare(const void* q, const void* kp, const void* vp, const void* kc, const
   prm.key_valid = key_valid;
   prm.Nq = Nq;
   prm.H = H;
-  prm.q_pairs = static_cast<int>(q_pairs);
+  prm.sc.n_units = static_cast<int>(n_units);
+  prm.sc.q_pairs = static_cast<int>(q_pairs);
+  prm.sc.H = H;
+  prm.sc.Nq = Nq;
   prm.n_tok[0] = Np;
   prm.n_tok[1] = Nc;
   prm.n_tiles[0] = (Np + ncp::BN - 1) / ncp::BN;
@@ -277,51 +311,26 @@ int noalloc_scratch(int dev, void** addr) {
 }
 
 // The schedule of launch<D> with the split workspace taken from the static
-// scratch: no allocation.  A schedule that would need more pieces than the
+// scratch: no allocation.  A schedule that would need more slots than the
 // scratch holds is refused (ATTN_ERR_SHAPE); the counters are cleared on the
 // stream first, since an aborted earlier call may have left them non-zero.
 template <int D>
 int launch_noalloc(Params& prm, long long n_units, cudaStream_t stream) {
   using C = ncp::Cfg<D>;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
-  static int sm_count[64] = {};
-  if (dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
-  if (sm_count[dev] == 0) {
-    int sms = 0;
-    if (cudaFuncSetAttribute(ncp::attn_fwd_kernel<D, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        sms < 1)
-      return ATTN_ERR_CUDA;
-    sm_count[dev] = sms;
-  }
-  const int sms = sm_count[dev];
+  int dev = 0, sms = 0;
+  if (configure<D, false>(&dev, &sms) != ATTN_OK) return ATTN_ERR_CUDA;
   const int T = prm.n_tiles[0] + prm.n_tiles[1];
-  const long long rem = n_units % sms;
-  long long pieces = 1;
-  if (rem > 0) {
-    pieces = sms / rem;
-    if (pieces > T / MIN_PIECE_TILES) pieces = T / MIN_PIECE_TILES;
-    if (pieces > MAX_PIECES) pieces = MAX_PIECES;
-  }
-  if (pieces < 2) pieces = 1;
-  const long long n_whole = pieces >= 2 ? n_units - rem : n_units;
-  const long long n_items = n_whole + (n_units - n_whole) * pieces;
-  if (n_items > 0x7fffffffLL) return ATTN_ERR_SHAPE;
-  if ((n_units - n_whole) * pieces > ncp::NOALLOC_PIECES) return ATTN_ERR_SHAPE;
+  const int grid = make_sched(prm.sc, n_units, T, sms, true);
+  if (sched_slots(prm.sc) > ncp::NOALLOC_SLOTS || 2 * prm.sc.tail_units > ncp::NOALLOC_COUNTERS)
+    return ATTN_ERR_SHAPE;
   void* scratch = nullptr;
   if (noalloc_scratch(dev, &scratch) != ATTN_OK) return ATTN_ERR_CUDA;
-  if (pieces >= 2 &&
+  if (prm.sc.tail_ctas > 0 &&
       cudaMemsetAsync(scratch, 0, ncp::NOALLOC_COUNT_BYTES, stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  prm.n_whole = static_cast<int>(n_whole);
-  prm.n_items = static_cast<int>(n_items);
-  prm.pieces = static_cast<int>(pieces);
   prm.ws_count = static_cast<unsigned int*>(scratch);
   prm.ws_part = reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) +
                                          ncp::NOALLOC_COUNT_BYTES);
-  const int grid = n_items < sms ? static_cast<int>(n_items) : sms;
   ncp::attn_fwd_kernel<D, false><<<grid, ncp::NUM_THREADS, C::SMEM_BYTES, stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -445,6 +454,36 @@ int attn_debug_exp2(const float* x, float* y, long long n, int mode, cudaStream_
   if (blocks > 0x7fffffffLL) return ATTN_ERR_SHAPE;
   ncp::exp2_probe_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(x, y, n, mode);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_debug_schedule(int B, int Nq, int H, int n_key_tiles, int sms, int masked, int* rows,
+                        int cap, int* n_rows, int* grid_out, int* slots_out) {
+  if (!n_rows || !grid_out || !slots_out || (cap > 0 && !rows)) return ATTN_ERR_NULL;
+  if (B < 1 || Nq < 1 || H < 1 || n_key_tiles < 1 || sms < 1 || cap < 0) return ATTN_ERR_SHAPE;
+  const long long q_pairs = (static_cast<long long>(Nq) + 2 * ncp::BM - 1) / (2 * ncp::BM);
+  const long long n_units = static_cast<long long>(B) * H * q_pairs;
+  if (n_units > 0x7fffffffLL) return ATTN_ERR_SHAPE;
+  ncp::Sched s;
+  s.q_pairs = static_cast<int>(q_pairs);
+  s.H = H;
+  s.Nq = Nq;
+  const int grid = make_sched(s, n_units, n_key_tiles, sms, masked == 0);
+  long long count = 0;
+  ncp::Item it;
+  for (int c = 0; c < grid; ++c)
+    for (int n = 0; masked ? ncp::schedule_item<true>(s, n_key_tiles, grid, c, n, it)
+                           : ncp::schedule_item<false>(s, n_key_tiles, grid, c, n, it);
+         ++n, ++count) {
+      if (count >= cap) continue;
+      int* r = rows + 12 * count;
+      const int v[12] = {c, n, it.u.b, it.u.h, it.u.q0, it.u.two ? 1 : 0, it.t_begin, it.t_end,
+                         it.tail, it.piece, it.pieces, it.slot0};
+      for (int e = 0; e < 12; ++e) r[e] = v[e];
+    }
+  *n_rows = static_cast<int>(count < 0x7fffffffLL ? count : 0x7fffffffLL);
+  *grid_out = grid;
+  *slots_out = sched_slots(s);
+  return count <= cap ? ATTN_OK : ATTN_ERR_SHAPE;
 }
 
 int attn_debug_set_fault(int mode, unsigned int wait_limit_us) {

@@ -79,6 +79,17 @@ struct SharedCtl {
   int abort_flag;
 };
 
+// Work schedule of one launch.  Units are (b, h, pair of 128-row query
+// tiles), n_units = B * H * q_pairs of them; see schedule_item.
+struct Sched {
+  int n_units;
+  int q_pairs;     // ceil(Nq / 256): units per (b, h); q pair fastest
+  int H, Nq;
+  int n_whole;     // units walked whole
+  int tail_units;  // units after them, cut into key ranges (0: none)
+  int tail_ctas;   // CTAs sharing the tail (0: no tail)
+};
+
 struct Params {
   CUtensorMap tm_q;
   CUtensorMap tm_k[2];   // [0] prefix segment, [1] current segment
@@ -90,16 +101,9 @@ struct Params {
   const int* image_ids;
   const unsigned char* key_valid;
   int Nq, H;
-  int q_pairs;           // ceil(Nq / 256): units per (b, h); units are (b, h, q pair), q pair fastest
-  // Work items, walked round-robin by the persistent CTAs: items [0, n_whole)
-  // are whole units; the units of the last, partly filled round are cut into
-  // `pieces` key ranges each (items n_whole + r * pieces + k), merged through
-  // the workspace by whichever piece of a unit finishes last.
-  int n_items;
-  int n_whole;
-  int pieces;
-  float* ws_part;          // [split unit][piece][query tile][128 rows][D + 4]: O, m, l
-  unsigned int* ws_count;  // [split unit][query tile] finished pieces (reset by the merger)
+  Sched sc;
+  float* ws_part;          // [piece slot][query tile][D / 4 + 1][128 rows][4]: O, then m, l
+  unsigned int* ws_count;  // [tail unit][query tile] finished pieces (reset by the merger)
   int n_tok[2];          // tokens per key segment
   int n_tiles[2];        // KV tiles per key segment
   float scale_log2;      // D^-0.5 * log2(e)
@@ -108,67 +112,96 @@ struct Params {
 };
 
 // ----------------------------------------------------------------------------
-// Work units and the softmax of one score tile
+// Work units and items
 // ----------------------------------------------------------------------------
 struct Unit {
   int b, h, q0;
   bool two;  // the second 128-row query tile has at least one row
 };
 
-template <bool BC>
-__device__ __forceinline__ Unit decode_unit(const Params& p, int unit) {
+__host__ __device__ __forceinline__ Unit decode_unit(const Sched& s, bool bc, int unit) {
   Unit u;
   // Dense forms: query pair fastest, so the CTAs running at one time share
   // the K/V of a few heads in L2.  Masked forms: rows see more keys the later
   // they sit, so hand out the last query pairs first, over all heads (longest
   // work first; all heads' K/V stay in L2 at these lengths).
-  const int n_bh = p.H * (p.n_items / (p.q_pairs * p.H));  // B * H (masked forms never split)
-  const int qp = BC ? p.q_pairs - 1 - unit / n_bh : unit % p.q_pairs;
-  const int bh = BC ? unit % n_bh : unit / p.q_pairs;
-  u.h = bh % p.H;
-  u.b = bh / p.H;
+  const int n_bh = s.n_units / s.q_pairs;  // B * H
+  const int qp = bc ? s.q_pairs - 1 - unit / n_bh : unit % s.q_pairs;
+  const int bh = bc ? unit % n_bh : unit / s.q_pairs;
+  u.h = bh % s.H;
+  u.b = bh / s.H;
   u.q0 = qp * (2 * BM);
-  u.two = (u.q0 + BM) < p.Nq;
+  u.two = (u.q0 + BM) < s.Nq;
   return u;
 }
 
 struct Item {
   Unit u;
   int t_begin, t_end;  // key tiles [t_begin, t_end) of the concatenated key sequence
-  int split;           // -1: whole unit; else index of the split unit
-  int piece;
+  int tail;            // -1: a whole unit; else the tail unit this piece belongs to
+  int piece, pieces;   // this piece's index among the tail unit's pieces, and their count
+  int slot0;           // workspace slot of the tail unit's piece 0 (piece k: slot0 + k)
 };
 
-// The n-th item of this CTA.  Dense forms: round robin.  Masked forms (units
-// of unequal work, longest first): a snake, so that CTAs that took a long
-// unit in one round take a short one in the next.
+// Owner of key-tile position x of the tail (positions r * T + t over tail
+// units r): CTA c holds positions [c W / G, (c + 1) W / G).
+__host__ __device__ __forceinline__ long long tail_owner(long long x, long long W, long long G) {
+  return ((x + 1) * G - 1) / W;
+}
+
+// Item n of CTA c in a grid of g, or false past its last one.
+//
+// No tail (s.tail_ctas == 0): CTA c takes units n g + c, round robin (masked
+// forms: a snake, rounds alternating direction, so that a CTA that took a long
+// unit in one round takes a short one in the next).
+//
+// Tail: the n_whole = rounds * g first units go round robin; the key tiles of
+// the tail_units units left, W = tail_units * T of them in unit order, are
+// cut into tail_ctas equal ranges, one per CTA c < tail_ctas.  A range that
+// crosses a unit boundary gives its CTA one piece of each unit.  Each piece
+// leaves its partial (O, m, l) in workspace slot c + r (r: the tail unit),
+// which is unique: a CTA later in the order only meets later units.
 template <bool BC>
-__device__ __forceinline__ int item_at(int n) {
-  const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-  return n * g + ((BC && (n & 1)) ? g - 1 - c : c);
+__host__ __device__ __forceinline__ bool schedule_item(const Sched& s, int T, int g, int c, int n,
+                                                       Item& it) {
+  it.tail = -1;
+  it.piece = 0;
+  it.pieces = 1;
+  it.slot0 = 0;
+  it.t_begin = 0;
+  it.t_end = T;
+  if (BC || s.tail_ctas == 0) {  // masked forms never split
+    const int unit = n * g + ((BC && (n & 1)) ? g - 1 - c : c);
+    if (unit >= s.n_units) return false;
+    it.u = decode_unit(s, BC, unit);
+    return true;
+  }
+  const int rounds = s.n_whole / g;
+  if (n < rounds) {
+    it.u = decode_unit(s, false, n * g + c);
+    return true;
+  }
+  if (c >= s.tail_ctas) return false;
+  const long long W = static_cast<long long>(s.tail_units) * T, G = s.tail_ctas;
+  const long long lo = c * W / G, hi = (c + 1) * W / G;
+  const long long r = lo / T + (n - rounds);
+  if (r >= s.tail_units || r * T >= hi) return false;
+  const long long first = tail_owner(r * T, W, G);
+  const long long last = tail_owner((r + 1) * T - 1, W, G);
+  it.t_begin = static_cast<int>((lo > r * T ? lo : r * T) - r * T);
+  it.t_end = static_cast<int>((hi < (r + 1) * T ? hi : (r + 1) * T) - r * T);
+  it.tail = static_cast<int>(r);
+  it.piece = c - static_cast<int>(first);
+  it.pieces = static_cast<int>(last - first) + 1;
+  it.slot0 = static_cast<int>(first + r);
+  it.u = decode_unit(s, false, s.n_whole + static_cast<int>(r));
+  return true;
 }
 
 template <bool BC>
-__device__ __forceinline__ Item decode_item(const Params& p, int item, int T) {
-  Item it;
-  int unit;
-  if (item < p.n_whole) {
-    unit = item;
-    it.split = -1;
-    it.piece = 0;
-    it.t_begin = 0;
-    it.t_end = T;
-  } else {
-    const int r = (item - p.n_whole) / p.pieces;
-    const int k = (item - p.n_whole) % p.pieces;
-    unit = p.n_whole + r;
-    it.split = r;
-    it.piece = k;
-    it.t_begin = (k * T) / p.pieces;
-    it.t_end = ((k + 1) * T) / p.pieces;
-  }
-  it.u = decode_unit<BC>(p, unit);
-  return it;
+__device__ __forceinline__ bool get_item(const Params& p, int T, int n, Item& it) {
+  return schedule_item<BC>(p.sc, T, static_cast<int>(gridDim.x), static_cast<int>(blockIdx.x), n,
+                           it);
 }
 
 // Block-causal visibility (definition prefix_cached_block_causal_h32_d128_
@@ -398,6 +431,62 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, i
   }
 }
 
+// Merge of a tail unit's pieces for one row: `part` points at this row's
+// partial in piece 0's slot (piece k's is 2 (D / 4 + 1) 128 float4 further),
+// D / 4 groups of O then (m, l) in the next group, group-major (128 float4
+// apart).  Pieces are combined in piece order, so the result does not depend
+// on which piece finished last: the common maximum and the sum first, then O
+// in groups of 64 columns (16 loads in flight per piece), stored as bf16 to
+// `dst` (nullptr: a padding row, nothing stored).  Kept out of line so that
+// its registers do not weigh on the softmax loop's allocation.
+template <int D>
+__device__ __noinline__ void merge_pieces(const float4* part, int nk, uint4* dst) {
+  constexpr int NG = D / 4 + 1;
+  const size_t piece_stride = static_cast<size_t>(2) * NG * BM;
+  float m_all = -INFINITY;
+  for (int k = 0; k < nk; ++k) m_all = fmaxf(m_all, __ldcg(part + k * piece_stride + (D / 4) * BM).x);
+  float l_all = 0.f;
+  for (int k = 0; k < nk; ++k) {
+    const float4 ml = __ldcg(part + k * piece_stride + (D / 4) * BM);
+    l_all = fmaf(ml.y, ex2(ml.x - m_all), l_all);
+  }
+  const float inv_l = 1.f / l_all;
+  const uint64_t inv2 = pk2(inv_l, inv_l);
+#pragma unroll
+  for (int cg = 0; cg < D / 64; ++cg) {
+    float acc[64];
+#pragma unroll
+    for (int e = 0; e < 64; ++e) acc[e] = 0.f;
+    for (int k = 0; k < nk; ++k) {
+      const float4* src = part + k * piece_stride;
+      float4 v[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = __ldcg(src + (cg * 16 + e) * BM);
+      const float a = ex2(__ldcg(src + (D / 4) * BM).x - m_all);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        acc[4 * e] = fmaf(v[e].x, a, acc[4 * e]);
+        acc[4 * e + 1] = fmaf(v[e].y, a, acc[4 * e + 1]);
+        acc[4 * e + 2] = fmaf(v[e].z, a, acc[4 * e + 2]);
+        acc[4 * e + 3] = fmaf(v[e].w, a, acc[4 * e + 3]);
+      }
+    }
+    if (dst) {
+#pragma unroll
+      for (int c = 0; c < 64; c += 8) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float o0, o1;
+          up2(fmul2(pk2(acc[c + 2 * e], acc[c + 2 * e + 1]), inv2), o0, o1);
+          w[e] = pack_bf16x2(o0, o1);
+        }
+        dst[(cg * 64 + c) / 8] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+  }
+}
+
 // ----------------------------------------------------------------------------
 // The kernel
 // ----------------------------------------------------------------------------
@@ -422,7 +511,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int T0 = p.n_tiles[0];
   const int T = T0 + p.n_tiles[1];
   const uint64_t limit = p.wait_limit_ns;
-  const int n_items = p.n_items;
 
   const uint32_t ring = base_u32 + C::RING_OFF;
   const uint32_t qs = base_u32 + C::Q_OFF;
@@ -514,10 +602,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       int slot = 0;
       uint32_t phase = 0;
-      int n = 0;  // units done by this CTA
       bool ok = true;
-      for (int item = item_at<BC>(0); item < n_items && ok; item = item_at<BC>(++n)) {
-        const Item it = decode_item<BC>(p, item, T);
+      Item it;
+      for (int n = 0; ok && get_item<BC>(p, T, n, it); ++n) {
         const Unit& u = it.u;
         // The Q buffers are free once every S MMA of the previous item is done.
         if (n > 0) {
@@ -538,7 +625,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int kind = 0; kind < 2; ++kind) {
             ok = wait_bounded(bar_kv_empty(slot), phase ^ 1u, limit, abort_flag, 1);
             if (!ok) break;
-            const bool skip = (p.fault_mode == 1) && kind == 1 && t == 1 && item == 0;
+            const bool skip = (p.fault_mode == 1) && kind == 1 && t == 1 && n == 0 && blockIdx.x == 0;
             if (!skip) {
               const CUtensorMap* map = kind == 0 ? &p.tm_k[seg] : &p.tm_v[seg];
               mbar_expect_tx(bar_kv_full(slot), C::TILE_BYTES);
@@ -588,7 +675,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t sc[2] = {0u, 0u};  // S commits per query tile (phases of s_full / p_full)
       uint32_t oc[2] = {0u, 0u};  // units finished per query tile (phases of o_full / o_free)
       bool ok = true;
-      int n = 0;
       // The first P V of a unit overwrites O_i: wait until the epilogue of the
       // previous unit has read it out of TMEM.
       auto pv = [&](int i, int v_slot, bool accumulate) -> bool {
@@ -600,8 +686,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         issue_pv(i, v_slot, accumulate);
         return true;
       };
-      for (int item = item_at<BC>(0); item < n_items && ok; item = item_at<BC>(++n)) {
-        const Item it = decode_item<BC>(p, item, T);
+      Item it;
+      for (int n = 0; ok && get_item<BC>(p, T, n, it); ++n) {
         const int nq = it.u.two ? 2 : 1;
         ok = wait_bounded(bar_q, n & 1, limit, abort_flag, 2);
         if (!ok) break;
@@ -659,8 +745,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t bar_part = smem_u32(&ctl->part_done[i]);
     const uint32_t bar_merge = smem_u32(&ctl->merge_ready[i]);
     const int row = wq * 32 + lane;  // row of the 128-row query tile (= TMEM lane)
-    for (int n = 0, item = item_at<BC>(0); item < n_items && ok; item = item_at<BC>(++n)) {
-      const Item it = decode_item<BC>(p, item, T);
+    Item it;
+    for (int n = 0; ok && get_item<BC>(p, T, n, it); ++n) {
       const Unit& u = it.u;
       if (i == 1 && !u.two) continue;
       float m = -INFINITY;  // running (possibly stale) maximum, log2 units
@@ -710,73 +796,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ofree[i]);
 
-      if (it.split >= 0) {
-        // A piece of a split unit: publish (O, m, l) of this row, count the
-        // piece in; the last piece of the unit merges every piece.
-        constexpr int RS = D + 4;  // row stride in floats (16-byte aligned)
-        const size_t tile_rows = static_cast<size_t>(2) * BM;
-        float* part_base = p.ws_part + static_cast<size_t>(it.split) * p.pieces * tile_rows * RS;
-        auto part_row = [&](int k) {
-          return part_base + ((static_cast<size_t>(k) * 2 + i) * BM + row) * RS;
+      const int q = u.q0 + i * BM + row;  // this thread's query row
+      uint4* dst = reinterpret_cast<uint4*>(
+          p.out + ((static_cast<size_t>(u.b) * p.Nq + q) * p.H + u.h) * D);
+      if (it.tail >= 0) {
+        // A piece of a tail unit: publish (O, m, l) of this row, count the
+        // piece in; the last piece of the unit to arrive merges every piece.
+        // A piece's partial for one query tile is D / 4 + 1 groups of four
+        // floats per row, group-major (group g of row r at g * 128 + r; the
+        // last group holds m and l), so a warp's access to one group is 512
+        // contiguous bytes.
+        constexpr int NG = D / 4 + 1;
+        auto part = [&](int k) {
+          return reinterpret_cast<float4*>(p.ws_part) +
+                 (static_cast<size_t>(it.slot0 + k) * 2 + i) * NG * BM + row;
         };
         {
-          float4* dst = reinterpret_cast<float4*>(part_row(it.piece));
+          float4* w = part(it.piece);
 #pragma unroll
-          for (int c = 0; c < D; c += 4)
-            __stcg(dst + c / 4, make_float4(__uint_as_float(r[c]), __uint_as_float(r[c + 1]),
-                                            __uint_as_float(r[c + 2]), __uint_as_float(r[c + 3])));
-          __stcg(dst + D / 4, make_float4(m, l, 0.f, 0.f));
+          for (int g = 0; g < D / 4; ++g)
+            __stcg(w + g * BM, make_float4(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1]),
+                                           __uint_as_float(r[4 * g + 2]),
+                                           __uint_as_float(r[4 * g + 3])));
+          __stcg(w + (D / 4) * BM, make_float4(m, l, 0.f, 0.f));
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_part);
-        if (wq == 0 && lane == 0) {
-          ok = wait_bounded(bar_part, mc & 1u, limit, abort_flag, 10);
-          if (ok) {
-            __threadfence();
-            const unsigned int before = atomicAdd(p.ws_count + it.split * 2 + i, 1u);
-            const int last = before == static_cast<unsigned int>(p.pieces - 1);
-            if (last) {
-              __threadfence();
-              atomicExch(p.ws_count + it.split * 2 + i, 0u);  // ready for the next launch
-            }
+        // The first warp of the tile counts the piece in.  It waits as a whole
+        // warp: a lane spinning on one barrier while another lane of the same
+        // warp spins on a different one serialises the two, and the waits
+        // then run up to the hardware's suspend limit in turn.
+        if (wq == 0) {
+          ok = warp_wait(bar_part, mc & 1u, limit, abort_flag, 10);
+          if (ok && lane == 0) {
+            // Release this tile's partial (the other warps' writes were
+            // acquired through bar_part) and, if last, acquire every piece's.
+            unsigned int* counter = p.ws_count + it.tail * 2 + i;
+            const unsigned int before = atom_add_acq_rel_gpu(counter, 1u);
+            const int last = before == static_cast<unsigned int>(it.pieces - 1);
+            if (last) atomicExch(counter, 0u);  // ready for the next launch
             ctl->last[i] = last;
             mbar_arrive(bar_merge);
           }
+          __syncwarp();
         }
         ok = warp_wait(bar_merge, mc & 1u, limit, abort_flag, 11);
         ++mc;
         if (!ok) break;
         if (!*reinterpret_cast<volatile int*>(&ctl->last[i])) continue;
-        // Merge every piece (this one's included, read back) in piece order,
-        // so the result does not depend on which piece finished last.
-        float m_all = -INFINITY;
-        for (int k = 0; k < p.pieces; ++k) m_all = fmaxf(m_all, __ldcg(part_row(k) + D));
-        l = 0.f;
-#pragma unroll
-        for (int c = 0; c < D; ++c) r[c] = 0u;
-        for (int k = 0; k < p.pieces; ++k) {
-          const float4* src4 = reinterpret_cast<const float4*>(part_row(k));
-          const float4 ml = __ldcg(src4 + D / 4);
-          const float a = ex2(ml.x - m_all);
-          l = fmaf(ml.y, a, l);
-#pragma unroll
-          for (int c = 0; c < D; c += 4) {
-            const float4 v = __ldcg(src4 + c / 4);
-            r[c] = __float_as_uint(fmaf(v.x, a, __uint_as_float(r[c])));
-            r[c + 1] = __float_as_uint(fmaf(v.y, a, __uint_as_float(r[c + 1])));
-            r[c + 2] = __float_as_uint(fmaf(v.z, a, __uint_as_float(r[c + 2])));
-            r[c + 3] = __float_as_uint(fmaf(v.w, a, __uint_as_float(r[c + 3])));
-          }
-        }
+        merge_pieces<D>(reinterpret_cast<const float4*>(p.ws_part) +
+                            static_cast<size_t>(it.slot0 * 2 + i) * (D / 4 + 1) * BM + row,
+                        it.pieces, q < p.Nq ? dst : nullptr);
+        continue;
       }
 
-      // O / l -> bf16 -> this thread's output row.
-      const int q = u.q0 + i * BM + row;
+      // A whole unit: O / l -> bf16 -> this thread's output row.
       if (q < p.Nq) {
         const float inv_l = 1.f / l;
         const uint64_t inv2 = pk2(inv_l, inv_l);
-        uint4* dst = reinterpret_cast<uint4*>(
-            p.out + ((static_cast<size_t>(u.b) * p.Nq + q) * p.H + u.h) * D);
 #pragma unroll
         for (int c = 0; c < D; c += 8) {
           uint32_t w[4];
