@@ -191,23 +191,28 @@ int attn_debug_set_fault(int mode, unsigned int wait_limit_us);
 int attn_debug_exp2(const float *x, float *y, long long n, int mode, cudaStream_t stream);
 
 /*
- * Test hook: the work schedule of a dense-family launch (masked = 0: dense,
- * cross, prefix-cached; masked = 1: block-causal and masked prefix forms),
- * computed on the host without a GPU.  A launch over B batches, Nq queries,
- * H heads and n_key_tiles key tiles of 128 on a GPU with `sms` SMs runs
- * *grid_out persistent CTAs; each item of each CTA is one row of 12 ints:
+ * Test hook: the work schedule of a launch, computed on the host without a
+ * GPU.  masked = 0: the dense family (dense, cross, prefix-cached) with
+ * n_key_tiles key tiles of 128 (image_ids and Np ignored).  masked = 1: the
+ * block-causal and masked prefix forms, Np prefix positions then Nq current
+ * ones, image_ids a host array of Np + Nq ids (caller-owned; the key tiles
+ * are counted from Np and Nq, n_key_tiles is ignored).  A launch over B
+ * batches, Nq queries and H heads on a GPU with `sms` SMs runs *grid_out
+ * persistent CTAs; each item of each CTA is one row of 12 ints:
  *   cta, n (the CTA's n-th item), b, h, q0 (first query row of the unit's
  *   pair of 128-row tiles), two (the second tile has rows), t_begin, t_end
- *   (key tiles [t_begin, t_end)), tail (-1: a whole unit, else its tail
- *   unit), piece, pieces (this piece's index and the tail unit's piece
- *   count), slot0 (workspace slot of the tail unit's piece 0).
+ *   (key tiles [t_begin, t_end); masked forms visit only some of them), tail
+ *   (-1: a whole unit, else its tail unit), piece, pieces (this piece's index
+ *   and the tail unit's piece count), slot0 (workspace slot of the tail
+ *   unit's piece 0).
  * Rows go to `rows` (caller-owned host memory, cap rows of 12 ints);
  * *n_rows receives the item count, *slots_out the workspace slots used.
- * Returns ATTN_OK, ATTN_ERR_NULL, or ATTN_ERR_SHAPE (a size < 1, or more
- * than cap items: then only cap rows are written).
+ * Returns ATTN_OK, ATTN_ERR_NULL, or ATTN_ERR_SHAPE (a size out of range, or
+ * more than cap items: then only cap rows are written).
  */
-int attn_debug_schedule(int B, int Nq, int H, int n_key_tiles, int sms, int masked, int *rows,
-                        int cap, int *n_rows, int *grid_out, int *slots_out);
+int attn_debug_schedule(int B, int Nq, int H, int n_key_tiles, int sms, int masked,
+                        const int *image_ids, int Np, int *rows, int cap, int *n_rows,
+                        int *grid_out, int *slots_out);
 
 #ifdef __cplusplus
 }

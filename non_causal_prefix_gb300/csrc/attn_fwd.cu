@@ -23,6 +23,7 @@
 #include <cmath>
 #include <map>
 #include <mutex>
+#include <vector>
 #include <utility>
 
 #include "ncp_attn.h"
@@ -106,15 +107,11 @@ bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) !
 // round would leave SMs idle, their key tiles are shared out evenly over the
 // CTAs instead, each unit's pieces merged through a workspace.
 // ---------------------------------------------------------------------------
-// Most pieces one unit's merge reads (plus one for a range boundary).
-constexpr int MAX_PIECES = 8;
-// A piece pays a Q load, a pipeline fill and a partial write + merge: give
-// each tail CTA at least this many key tiles.
-constexpr int MIN_PIECE_TILES = 4;
-
-// Schedule of n_units units of T key tiles each on `sms` SMs; `can_split`
-// false (masked forms, whose units visit a data-dependent subset of the key
-// tiles, or no workspace) keeps every unit whole.  Returns the grid size.
+// Schedule of n_units units of (at most) T key tiles each on `sms` SMs;
+// `can_split` false (no workspace) keeps every unit whole.  The masked forms
+// visit a data-dependent subset of each unit's key tiles: T bounds their
+// work here, and the kernel shares out the tail by the tiles actually
+// visited.  Returns the grid size.
 int make_sched(ncp::Sched& s, long long n_units, int T, int sms, bool can_split) {
   s.n_units = static_cast<int>(n_units);
   s.n_whole = s.n_units;
@@ -124,9 +121,9 @@ int make_sched(ncp::Sched& s, long long n_units, int T, int sms, bool can_split)
   if (can_split && rem > 0) {
     const long long W = rem * T;
     long long g_tail = sms;
-    if (g_tail > W / MIN_PIECE_TILES) g_tail = W / MIN_PIECE_TILES;
-    if (g_tail > rem * MAX_PIECES) g_tail = rem * MAX_PIECES;
-    if (g_tail > rem) {
+    if (g_tail > W / ncp::MIN_PIECE_TILES) g_tail = W / ncp::MIN_PIECE_TILES;
+    if (g_tail > rem * ncp::MAX_PIECES) g_tail = rem * ncp::MAX_PIECES;
+    if (g_tail > rem && rem <= ncp::MAX_TAIL_UNITS) {
       s.n_whole = static_cast<int>(n_units - rem);
       s.tail_units = static_cast<int>(rem);
       s.tail_ctas = static_cast<int>(g_tail);
@@ -137,7 +134,7 @@ int make_sched(ncp::Sched& s, long long n_units, int T, int sms, bool can_split)
 }
 
 // Workspace slots a schedule uses: tail piece (CTA c, tail unit r) takes slot
-// c + r, so fewer than tail_ctas + tail_units.
+// c + r, so fewer than tail_ctas + tail_units (< 2 x SMs).
 int sched_slots(const ncp::Sched& s) { return s.tail_ctas ? s.tail_ctas + s.tail_units - 1 : 0; }
 
 // Bytes of partials for `slots` pieces: 2 query tiles x 128 rows x (128 + 4)
@@ -147,7 +144,7 @@ size_t part_bytes(long long slots) {
 }
 
 // ---------------------------------------------------------------------------
-// Split workspace: partials of the tail pieces (at most 2 x SMs slots) plus
+// Split workspace: partials of the tail pieces (2 x SMs slots) plus
 // one arrival counter per (tail unit, query tile).  One per (device, stream),
 // so calls that run concurrently on different streams never share one;
 // created on the first call that splits (cudaMalloc, then a zeroing memset on
@@ -220,7 +217,7 @@ int launch(Params& prm, long long n_units, cudaStream_t stream) {
   int dev = 0, sms = 0;
   if (configure<D, BC>(&dev, &sms) != ATTN_OK) return ATTN_ERR_CUDA;
   const int T = prm.n_tiles[0] + prm.n_tiles[1];
-  int grid = make_sched(prm.sc, n_units, T, sms, !BC);
+  int grid = make_sched(prm.sc, n_units, T, sms, true);
   const Workspace* ws = nullptr;
   if (prm.sc.tail_ctas > 0) {
     ws = get_workspace(dev, sms, stream);
@@ -456,23 +453,48 @@ int attn_debug_exp2(const float* x, float* y, long long n, int mode, cudaStream_
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_debug_schedule(int B, int Nq, int H, int n_key_tiles, int sms, int masked, int* rows,
-                        int cap, int* n_rows, int* grid_out, int* slots_out) {
+int attn_debug_schedule(int B, int Nq, int H, int n_key_tiles, int sms, int masked,
+                        const int* image_ids, int Np, int* rows, int cap, int* n_rows,
+                        int* grid_out, int* slots_out) {
   if (!n_rows || !grid_out || !slots_out || (cap > 0 && !rows)) return ATTN_ERR_NULL;
-  if (B < 1 || Nq < 1 || H < 1 || n_key_tiles < 1 || sms < 1 || cap < 0) return ATTN_ERR_SHAPE;
+  if (B < 1 || Nq < 1 || H < 1 || sms < 1 || cap < 0 || Np < 0) return ATTN_ERR_SHAPE;
+  ncp::Params prm{};
+  prm.Nq = Nq;
+  prm.H = H;
+  prm.n_tok[0] = masked ? Np : 0;
+  prm.n_tok[1] = Nq;
+  prm.n_tiles[0] = masked ? (Np + ncp::BN - 1) / ncp::BN : 0;
+  prm.n_tiles[1] = masked ? (Nq + ncp::BN - 1) / ncp::BN : n_key_tiles;
+  const int T = prm.n_tiles[0] + prm.n_tiles[1];
+  if (T < 1 || (masked && T > ncp::MAX_SEQ_TILES)) return ATTN_ERR_SHAPE;
   const long long q_pairs = (static_cast<long long>(Nq) + 2 * ncp::BM - 1) / (2 * ncp::BM);
   const long long n_units = static_cast<long long>(B) * H * q_pairs;
   if (n_units > 0x7fffffffLL) return ATTN_ERR_SHAPE;
-  ncp::Sched s;
+  ncp::Sched& s = prm.sc;
   s.q_pairs = static_cast<int>(q_pairs);
   s.H = H;
   s.Nq = Nq;
-  const int grid = make_sched(s, n_units, n_key_tiles, sms, masked == 0);
+  const int grid = make_sched(s, n_units, T, sms, true);
+  // Masked forms: the kernel's tile table and tail prefix sums, built here.
+  std::vector<int> table(3 * ncp::MAX_SEQ_TILES, 0), pre(s.tail_units + 1, 0);
+  ncp::MaskedTail mt{&prm, ncp::TileTable{table.data()}, pre.data()};
+  if (masked) {
+    if (!image_ids) return ATTN_ERR_NULL;
+    for (int t = 0; t < T; ++t)
+      ncp::tile_summary(prm, image_ids, t, table[t], table[ncp::MAX_SEQ_TILES + t],
+                        table[2 * ncp::MAX_SEQ_TILES + t]);
+    for (int r = 0; r < s.tail_units; ++r) {
+      const ncp::Unit u = ncp::decode_unit(s, true, s.n_whole + r);
+      int cnt = 0;
+      for (int t = 0; t < T; ++t) cnt += ncp::bc_unit_visits(mt.tt, prm, u, t) ? 1 : 0;
+      pre[r + 1] = pre[r] + cnt;
+    }
+  }
   long long count = 0;
   ncp::Item it;
   for (int c = 0; c < grid; ++c)
-    for (int n = 0; masked ? ncp::schedule_item<true>(s, n_key_tiles, grid, c, n, it)
-                           : ncp::schedule_item<false>(s, n_key_tiles, grid, c, n, it);
+    for (int n = 0; masked ? ncp::schedule_item<true>(s, T, grid, c, n, it, &mt)
+                           : ncp::schedule_item<false>(s, T, grid, c, n, it, nullptr);
          ++n, ++count) {
       if (count >= cap) continue;
       int* r = rows + 12 * count;

@@ -21,6 +21,13 @@ constexpr int MAX_SLOTS = 8;
 // Block-causal form: per-CTA table of the image ids in each 128-token tile
 // (min, max and "one image only"), held in shared memory; N <= 128 * this.
 constexpr int MAX_SEQ_TILES = 1024;
+// Split tail (see schedule_item): most pieces one merge reads (plus one for a
+// range boundary), least key tiles per tail CTA (a piece pays a Q load, a
+// pipeline fill and a partial write + merge), and most tail units (units in
+// a last, partly filled round: fewer than the SM count).
+constexpr int MAX_PIECES = 8;
+constexpr int MIN_PIECE_TILES = 4;
+constexpr int MAX_TAIL_UNITS = 1024;
 // Rescale O only when the running row maximum (log2 units) grows by more than
 // this; otherwise keep the stale maximum.  Exact, because the final 1/l uses
 // the same maximum as the accumulated O, and p <= 2^8 stays far from overflow.
@@ -50,8 +57,10 @@ struct Cfg {
   static constexpr uint32_t Q_OFF = RING_OFF + NSLOT * TILE_BYTES;
   static constexpr uint32_t BAR_OFF = Q_OFF + 2 * TILE_BYTES;
   static constexpr uint32_t SMEM_BYTES = BAR_OFF + 512 + 1024;  // barriers + 1 KiB alignment slack
-  static constexpr uint32_t SUM_OFF = BAR_OFF + 512;             // block-causal tile table
-  static constexpr uint32_t SMEM_BYTES_BC = SUM_OFF + 3 * 4 * MAX_SEQ_TILES + 1024;
+  static constexpr uint32_t SUM_OFF = BAR_OFF + 512;             // masked forms: tile table
+  static constexpr uint32_t TAIL_OFF = SUM_OFF + 3 * 4 * MAX_SEQ_TILES;  // and tail prefix sums
+  static constexpr uint32_t ITEMS_OFF = TAIL_OFF + 4 * (MAX_TAIL_UNITS + 4);  // and tail items
+  static constexpr uint32_t SMEM_BYTES_BC = ITEMS_OFF + 48 * 32 + 1024;
   // Share of the exponentials computed by the FMA-pipe polynomial instead of
   // the MUFU unit: POLY_NUM of every POLY_DEN packed pairs.  On GB300 the
   // MUFU unit does about 30 exp2 per clock per SM and the polynomial about 13:
@@ -75,6 +84,7 @@ struct SharedCtl {
   uint64_t merge_ready[2]; // the piece's arrival count is known (SharedCtl::last)
   uint64_t drain;
   int last[2];             // this piece is the last of its unit: merge and store
+  int n_tail_items;        // masked forms: tail items of this CTA kept in shared memory
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -143,84 +153,26 @@ struct Item {
   int slot0;           // workspace slot of the tail unit's piece 0 (piece k: slot0 + k)
 };
 
-// Owner of key-tile position x of the tail (positions r * T + t over tail
-// units r): CTA c holds positions [c W / G, (c + 1) W / G).
-__host__ __device__ __forceinline__ long long tail_owner(long long x, long long W, long long G) {
-  return ((x + 1) * G - 1) / W;
-}
-
-// Item n of CTA c in a grid of g, or false past its last one.
-//
-// No tail (s.tail_ctas == 0): CTA c takes units n g + c, round robin (masked
-// forms: a snake, rounds alternating direction, so that a CTA that took a long
-// unit in one round takes a short one in the next).
-//
-// Tail: the n_whole = rounds * g first units go round robin; the key tiles of
-// the tail_units units left, W = tail_units * T of them in unit order, are
-// cut into tail_ctas equal ranges, one per CTA c < tail_ctas.  A range that
-// crosses a unit boundary gives its CTA one piece of each unit.  Each piece
-// leaves its partial (O, m, l) in workspace slot c + r (r: the tail unit),
-// which is unique: a CTA later in the order only meets later units.
-template <bool BC>
-__host__ __device__ __forceinline__ bool schedule_item(const Sched& s, int T, int g, int c, int n,
-                                                       Item& it) {
-  it.tail = -1;
-  it.piece = 0;
-  it.pieces = 1;
-  it.slot0 = 0;
-  it.t_begin = 0;
-  it.t_end = T;
-  if (BC || s.tail_ctas == 0) {  // masked forms never split
-    const int unit = n * g + ((BC && (n & 1)) ? g - 1 - c : c);
-    if (unit >= s.n_units) return false;
-    it.u = decode_unit(s, BC, unit);
-    return true;
-  }
-  const int rounds = s.n_whole / g;
-  if (n < rounds) {
-    it.u = decode_unit(s, false, n * g + c);
-    return true;
-  }
-  if (c >= s.tail_ctas) return false;
-  const long long W = static_cast<long long>(s.tail_units) * T, G = s.tail_ctas;
-  const long long lo = c * W / G, hi = (c + 1) * W / G;
-  const long long r = lo / T + (n - rounds);
-  if (r >= s.tail_units || r * T >= hi) return false;
-  const long long first = tail_owner(r * T, W, G);
-  const long long last = tail_owner((r + 1) * T - 1, W, G);
-  it.t_begin = static_cast<int>((lo > r * T ? lo : r * T) - r * T);
-  it.t_end = static_cast<int>((hi < (r + 1) * T ? hi : (r + 1) * T) - r * T);
-  it.tail = static_cast<int>(r);
-  it.piece = c - static_cast<int>(first);
-  it.pieces = static_cast<int>(last - first) + 1;
-  it.slot0 = static_cast<int>(first + r);
-  it.u = decode_unit(s, false, s.n_whole + static_cast<int>(r));
-  return true;
-}
-
-template <bool BC>
-__device__ __forceinline__ bool get_item(const Params& p, int T, int n, Item& it) {
-  return schedule_item<BC>(p.sc, T, static_cast<int>(gridDim.x), static_cast<int>(blockIdx.x), n,
-                           it);
-}
-
 // Block-causal visibility (definition prefix_cached_block_causal_h32_d128_
 // prefix0): query i sees key j iff j <= i, or both carry the same image id >= 0.
 // Tiles are summarised by the range [lo, hi] of their non-negative ids (lo >
 // hi: text only) and by `uni` (every token in one image).
+// The three arrays sit back to back in shared memory (MAX_SEQ_TILES each),
+// reached from one base to keep the loops' live state small.
 struct TileTable {
-  const int* lo;
-  const int* hi;
-  const int* uni;
+  const int* base;
+  __host__ __device__ __forceinline__ int lo(int t) const { return base[t]; }
+  __host__ __device__ __forceinline__ int hi(int t) const { return base[MAX_SEQ_TILES + t]; }
+  __host__ __device__ __forceinline__ int uni(int t) const { return base[2 * MAX_SEQ_TILES + t]; }
 };
 
 // Key tiles walk the prefix segment (tiles [0, T0)) then the current one;
 // position of the first key of tile t, and its number of keys.
-__device__ __forceinline__ int key_tile_pos(const Params& p, int t) {
+__host__ __device__ __forceinline__ int key_tile_pos(const Params& p, int t) {
   const int T0 = p.n_tiles[0];
   return t < T0 ? t * BN : p.n_tok[0] + (t - T0) * BN;
 }
-__device__ __forceinline__ int key_tile_len(const Params& p, int t) {
+__host__ __device__ __forceinline__ int key_tile_len(const Params& p, int t) {
   const int T0 = p.n_tiles[0];
   const int seg = t < T0 ? 0 : 1;
   return min(BN, p.n_tok[seg] - (t - (seg ? T0 : 0)) * BN);
@@ -231,15 +183,15 @@ __device__ __forceinline__ int key_tile_len(const Params& p, int t) {
 // an image id both may share (their id ranges meet; the query tiles are the
 // current segment's tiles T0 + qt).  key_valid only removes keys, so the
 // filter stays exact: a skipped tile has no visible pair.
-__device__ __forceinline__ bool bc_unit_visits(const TileTable& tt, const Params& p, const Unit& u,
-                                               int t) {
+__host__ __device__ __forceinline__ bool bc_unit_visits(const TileTable& tt, const Params& p,
+                                                        const Unit& u, int t) {
   const int r_last = p.n_tok[0] + min(u.q0 + 2 * BM, p.Nq) - 1;
   if (key_tile_pos(p, t) <= r_last) return true;
   const int qt0 = p.n_tiles[0] + u.q0 / BM;
   const int qt1 = u.two ? qt0 + 1 : qt0;
-  const int qlo = min(tt.lo[qt0], tt.lo[qt1]);
-  const int qhi = max(tt.hi[qt0], tt.hi[qt1]);
-  return qlo <= tt.hi[t] && tt.lo[t] <= qhi;
+  const int qlo = min(tt.lo(qt0), tt.lo(qt1));
+  const int qhi = max(tt.hi(qt0), tt.hi(qt1));
+  return qlo <= tt.hi(t) && tt.lo(t) <= qhi;
 }
 
 // Every query row of query tile qt (current-segment tile T0 + qt, first row
@@ -250,16 +202,186 @@ __device__ __forceinline__ bool bc_tile_full(const TileTable& tt, const Params& 
                                              int q_first, int t) {
   if (key_tile_pos(p, t) + key_tile_len(p, t) - 1 <= p.n_tok[0] + q_first) return true;
   const int tq = p.n_tiles[0] + qt;
-  return tt.uni[tq] && tt.uni[t] && tt.lo[tq] == tt.lo[t];
+  return tt.uni(tq) && tt.uni(t) && tt.lo(tq) == tt.lo(t);
+}
+
+// Owner of tail position x (tail positions in unit order): CTA c of G holds
+// positions [c W / G, (c + 1) W / G).
+__host__ __device__ __forceinline__ long long tail_owner(long long x, long long W, long long G) {
+  return ((x + 1) * G - 1) / W;
+}
+
+// Summary of the image ids of key tile t of the masked forms (see TileTable),
+// one thread's version (the kernel builds its table warp by warp).
+__host__ __device__ inline void tile_summary(const Params& p, const int* ids, int t, int& lo,
+                                             int& hi, int& uni) {
+  lo = 0x7fffffff;
+  hi = -1;
+  bool text = false;
+  const int pos0 = key_tile_pos(p, t), len = key_tile_len(p, t);
+  for (int e = 0; e < len; ++e) {
+    const int id = ids[pos0 + e];
+    if (id < 0) {
+      text = true;
+    } else {
+      lo = id < lo ? id : lo;
+      hi = id > hi ? id : hi;
+    }
+  }
+  uni = (!text && lo == hi) ? 1 : 0;
+}
+
+// Masked forms' tail: the key-tile table, and pre[r] = key tiles visited by
+// the tail units before tail unit r (pre[tail_units]: all of them).
+// items[0 .. n_items) (kernel only): this CTA's first tail items, worked out
+// once at the start of the kernel.
+struct MaskedTail {
+  const Params* p;
+  TileTable tt;
+  const int* pre;
+  const Item* items;
+  int n_items;
+};
+
+// Most tail items of one CTA kept in shared memory (later ones, rare, are
+// worked out when reached).
+constexpr int MAX_CTA_TAIL_ITEMS = 32;
+static_assert(sizeof(Item) <= 48, "tail item list: 48 bytes per item in shared memory");
+
+// CTAs sharing a masked tail of W visited tiles: at most the launch's
+// tail_ctas, and at least MIN_PIECE_TILES visited tiles each.
+__host__ __device__ __forceinline__ long long masked_tail_ctas(const Sched& s, long long W) {
+  long long G = W / MIN_PIECE_TILES;
+  if (G > s.tail_ctas) G = s.tail_ctas;
+  return G < 1 ? 1 : G;
+}
+
+// Fill `it` with the tail piece of tail unit r that covers tail positions
+// [lo, hi) clipped to the unit's [u0, u1), positions held by CTAs of G over
+// W; `base`: the unit's first position.  to_tile maps a position inside the
+// unit to its key tile (identity for the dense forms).
+template <class ToTile>
+__host__ __device__ __forceinline__ void tail_piece(const Sched& s, bool bc, int c, long long r,
+                                                    long long lo, long long hi, long long u0,
+                                                    long long u1, long long W, long long G,
+                                                    ToTile to_tile, Item& it) {
+  const long long first = tail_owner(u0, W, G);
+  const long long last = tail_owner(u1 - 1, W, G);
+  const int v0 = static_cast<int>((lo > u0 ? lo : u0) - u0);
+  const int v1 = static_cast<int>((hi < u1 ? hi : u1) - u0);
+  it.u = decode_unit(s, bc, s.n_whole + static_cast<int>(r));
+  it.t_begin = to_tile(it.u, v0);
+  it.t_end = to_tile(it.u, v1 - 1) + 1;
+  if (first == last) {  // the whole unit in one range: no merge
+    it.tail = -1;
+    it.piece = 0;
+    it.pieces = 1;
+    it.slot0 = 0;
+  } else {
+    it.tail = static_cast<int>(r);
+    it.piece = c - static_cast<int>(first);
+    it.pieces = static_cast<int>(last - first) + 1;
+    it.slot0 = static_cast<int>(first + r);
+  }
+}
+
+// Tail item j of CTA c of the masked forms (see schedule_item); to_tile(u,
+// v) gives the v-th key tile unit u visits.
+template <class ToTile>
+__host__ __device__ __forceinline__ bool masked_tail_item(const Sched& s, const MaskedTail& mt,
+                                                          int T, int c, int j, Item& it,
+                                                          ToTile to_tile) {
+  const int* pre = mt.pre;
+  const long long W = pre[s.tail_units], G = masked_tail_ctas(s, W);
+  if (c >= G) return false;
+  const long long lo = c * W / G, hi = (c + 1) * W / G;
+  if (lo >= hi) return false;
+  // The tail unit holding position lo: the last r with pre[r] <= lo (pre
+  // rises strictly: every unit visits its diagonal tiles).
+  int a = 0, b = s.tail_units - 1;
+  while (a < b) {
+    const int mid = (a + b + 1) / 2;
+    if (pre[mid] <= lo) a = mid; else b = mid - 1;
+  }
+  const int r = a + j;
+  if (r >= s.tail_units || pre[r] >= hi) return false;
+  tail_piece(s, true, c, r, lo, hi, pre[r], pre[r + 1], W, G, to_tile, it);
+  return true;
+}
+
+// Item n of CTA c in a grid of g, or false past its last one.
+//
+// No tail (s.tail_ctas == 0): CTA c takes units n g + c, round robin (masked
+// forms: a snake, rounds alternating direction, so that a CTA that took a long
+// unit in one round takes a short one in the next).
+//
+// Tail: the n_whole = rounds * g first units go the same way; the work of the
+// tail_units units left is laid out in unit order as W tail positions and cut
+// into G equal ranges, one per CTA c < G.  Dense forms: a position is a key
+// tile, W = tail_units * T, G = tail_ctas.  Masked forms: a position is a
+// *visited* key tile (mt->pre counts them), G = masked_tail_ctas(W).  A range
+// that crosses a unit boundary gives its CTA one piece of each unit.  Each
+// piece leaves its partial (O, m, l) in workspace slot c + r (r: the tail
+// unit), which is unique: a CTA later in the order only meets later units.
+template <bool BC>
+__host__ __device__ __forceinline__ bool schedule_item(const Sched& s, int T, int g, int c, int n,
+                                                       Item& it, const MaskedTail* mt) {
+  it.tail = -1;
+  it.piece = 0;
+  it.pieces = 1;
+  it.slot0 = 0;
+  it.t_begin = 0;
+  it.t_end = T;
+  const int rounds = s.tail_ctas ? s.n_whole / g : 0;
+  if (s.tail_ctas == 0 || n < rounds) {
+    const int unit = n * g + ((BC && (n & 1)) ? g - 1 - c : c);
+    if (unit >= s.n_whole) return false;
+    it.u = decode_unit(s, BC, unit);
+    return true;
+  }
+  const int j = n - rounds;  // tail item of this CTA
+  if (!BC) {
+    const long long W = static_cast<long long>(s.tail_units) * T, G = s.tail_ctas;
+    if (c >= G) return false;
+    const long long lo = c * W / G, hi = (c + 1) * W / G;
+    const long long r = lo / T + j;
+    if (r >= s.tail_units || r * T >= hi) return false;
+    tail_piece(s, false, c, r, lo, hi, r * T, (r + 1) * T, W, G,
+               [](const Unit&, int v) { return v; }, it);
+    return true;
+  }
+  return masked_tail_item(s, *mt, T, c, j, it, [&](const Unit& u, int v) {
+    int seen = 0;
+    for (int t = 0; t < T; ++t)
+      if (bc_unit_visits(mt->tt, *mt->p, u, t) && seen++ == v) return t;
+    return T - 1;
+  });
+}
+
+template <bool BC>
+__device__ __forceinline__ bool get_item(const Params& p, const MaskedTail* mt, int T, int n,
+                                         Item& it) {
+  if (BC && p.sc.tail_ctas > 0) {
+    const int j = n - p.sc.n_whole / static_cast<int>(gridDim.x);
+    if (j >= 0 && j < mt->n_items) {
+      it = mt->items[j];
+      return true;
+    }
+    if (j >= 0 && j < MAX_CTA_TAIL_ITEMS) return false;  // the list holds every item
+  }
+  return schedule_item<BC>(p.sc, T, static_cast<int>(gridDim.x), static_cast<int>(blockIdx.x), n,
+                           it, mt);
 }
 
 // Per-row mask of one key tile of the masked forms: key position c0 + c is
 // visible to the query at position qi (image id idq) iff c0 + c <= qi or its
-// id equals idq >= 0, and (with key_valid) the key is valid.
+// id equals idq >= 0, and (with key_valid, batch b) the key is valid.  The
+// id and flag pointers are formed from the kernel parameters where they are
+// read, so that they are not live across the key loop.
 struct RowMask {
-  const int* ids;  // image ids of the tile's keys (ids[0] is key c0); nullptr: all visible
-  const unsigned char* valid;  // key_valid of the tile's keys for this batch; nullptr: all valid
-  int c0, qi, idq, n;  // n: key positions (Np + Nq; nothing past n is read)
+  int c0, qi, idq, b;
+  bool ids;    // test image ids (false: every key of the tile visible)
+  bool valid;  // test key_valid (false: every key valid)
 };
 
 // One 128-key tile of the online softmax for this thread's query row:
@@ -267,71 +389,62 @@ struct RowMask {
 // over the first 64 columns of S; O is rescaled in TMEM when m moved.
 template <int D, bool BC>
 __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, int valid, float sl2,
-                                             bool may_rescale, const RowMask& mask, float& m,
-                                             float& l) {
+                                             bool may_rescale, const Params& p,
+                                             const RowMask& mask, float& m, float& l) {
+  const int n_keys = p.n_tok[0] + p.n_tok[1];  // key positions (nothing past them is read)
   // Masked forms: this row's visibility of the tile's 128 keys as a bitmask,
-  // built before the scores are loaded so that fewer registers are live.
+  // built before the scores are loaded so that fewer registers are live.  The
+  // warp builds it together (the flags are warp-uniform): lane l reads the
+  // ids and flags of keys l, 32 + l, 64 + l, 96 + l (coalesced), so that one
+  // ballot per 32 keys gives a mask word in key order.
   uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
   bool masked = false;
+  const int lane = static_cast<int>(threadIdx.x & 31u);
   if (BC && mask.ids) {
     masked = true;
-    const int lim = mask.qi - mask.c0;  // keys c <= lim are visible causally
-    const bool img = mask.idq >= 0;
-    if (mask.c0 + BN <= mask.n && (mask.c0 & 3) == 0) {
-      const int4* ids4 = reinterpret_cast<const int4*>(mask.ids);
+    const int* ids = p.image_ids + mask.c0;
+    int kid[4];  // keys past the last position read as text; `valid` masks them
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        uint32_t w = 0;
+    for (int e = 0; e < 4; ++e) {
+      const int c = 32 * e + lane;
+      kid[e] = (mask.c0 + c < n_keys) ? __ldg(ids + c) : -1;
+    }
+    // Causal part: keys c <= qi - c0.
+    const int lim = mask.qi - mask.c0;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int4 id = __ldg(ids4 + 8 * g + k);
-          const int c = 32 * g + 4 * k;
-          w |= static_cast<uint32_t>(c + 0 <= lim || (img && id.x == mask.idq)) << (4 * k + 0);
-          w |= static_cast<uint32_t>(c + 1 <= lim || (img && id.y == mask.idq)) << (4 * k + 1);
-          w |= static_cast<uint32_t>(c + 2 <= lim || (img && id.z == mask.idq)) << (4 * k + 2);
-          w |= static_cast<uint32_t>(c + 3 <= lim || (img && id.w == mask.idq)) << (4 * k + 3);
-        }
-        vis[g] = w;
+    for (int e = 0; e < 4; ++e) {
+      const int d = lim - 32 * e;  // keys 32 e .. 32 e + d of this word
+      vis[e] = d >= 31 ? ~0u : (d < 0 ? 0u : (2u << d) - 1u);
+    }
+    // Image part, once per distinct image id among the warp's rows.
+    uint32_t pending = __ballot_sync(0xffffffffu, mask.idq >= 0);
+    while (pending) {
+      const int X = __shfl_sync(0xffffffffu, mask.idq, __ffs(pending) - 1);
+      const bool mine = mask.idq == X;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t w = __ballot_sync(0xffffffffu, kid[e] == X);
+        if (mine) vis[e] |= w;
       }
-    } else {
-      // Last tile of the sequence, or ids not 16-byte aligned: one by one.
-      // Keys past n are masked by `valid` below.
-#pragma unroll
-      for (int c = 0; c < BN; ++c) {
-        const int id = (mask.c0 + c < mask.n) ? __ldg(mask.ids + c) : -1;
-        if (!(c <= lim || (img && id == mask.idq))) vis[c / 32] &= ~(1u << (c % 32));
-      }
+      pending &= ~__ballot_sync(0xffffffffu, mine);
     }
   }
   if (BC && mask.valid) {
-    if (mask.c0 + BN <= mask.n && (reinterpret_cast<uintptr_t>(mask.valid) & 15u) == 0) {
-      // 128 flags as eight 16-byte loads; the per-key pass runs only when a
-      // flag is zero (zero-byte test per 32-bit word).
-      const uint4* kv4 = reinterpret_cast<const uint4*>(mask.valid);
-      uint32_t zero = 0;
+    // key_valid, the same for every row: keys past the last position count
+    // as valid here (`valid` masks them).
+    const unsigned char* kv = p.key_valid + static_cast<size_t>(mask.b) * n_keys + mask.c0;
+    uint32_t okw[4];
+    bool all = true;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint4 v = __ldg(kv4 + k);
-        zero |= ((v.x - 0x01010101u) & ~v.x) | ((v.y - 0x01010101u) & ~v.y) |
-                ((v.z - 0x01010101u) & ~v.z) | ((v.w - 0x01010101u) & ~v.w);
-      }
-      if (zero & 0x80808080u) {
-        masked = true;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint4 v = __ldg(kv4 + k);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int c = 0; c < 16; ++c)
-            if (((w[c / 4] >> (8 * (c % 4))) & 0xffu) == 0)
-              vis[(16 * k + c) / 32] &= ~(1u << ((16 * k + c) % 32));
-        }
-      }
-    } else {
+    for (int e = 0; e < 4; ++e) {
+      const int c = 32 * e + lane;
+      okw[e] = __ballot_sync(0xffffffffu, mask.c0 + c >= n_keys || __ldg(kv + c) != 0);
+      all = all && okw[e] == ~0u;
+    }
+    if (!all) {
       masked = true;
 #pragma unroll
-      for (int c = 0; c < BN; ++c)
-        if (mask.c0 + c < mask.n && __ldg(mask.valid + c) == 0) vis[c / 32] &= ~(1u << (c % 32));
+      for (int e = 0; e < 4; ++e) vis[e] &= okw[e];
     }
   }
   float s[BN];
@@ -518,10 +631,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t bar_qfree = smem_u32(&ctl->q_free);
   auto bar_kv_full = [&](int s) { return smem_u32(&ctl->kv_full[s]); };
   auto bar_kv_empty = [&](int s) { return smem_u32(&ctl->kv_empty[s]); };
-  const uint32_t bar_s[2] = {smem_u32(&ctl->s_full[0]), smem_u32(&ctl->s_full[1])};
-  const uint32_t bar_p[2] = {smem_u32(&ctl->p_full[0]), smem_u32(&ctl->p_full[1])};
-  const uint32_t bar_o[2] = {smem_u32(&ctl->o_full[0]), smem_u32(&ctl->o_full[1])};
-  const uint32_t bar_ofree[2] = {smem_u32(&ctl->o_free[0]), smem_u32(&ctl->o_free[1])};
+  // Per query tile (addresses computed, not indexed from an array: a runtime
+  // index into a local array would put it in local memory).
+  auto bar_s = [&](int i) { return smem_u32(&ctl->s_full[i]); };
+  auto bar_p = [&](int i) { return smem_u32(&ctl->p_full[i]); };
+  auto bar_o = [&](int i) { return smem_u32(&ctl->o_full[i]); };
+  auto bar_ofree = [&](int i) { return smem_u32(&ctl->o_free[i]); };
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
@@ -531,10 +646,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(bar_kv_empty(s), 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar_s[i], 1);
-      mbar_init(bar_p[i], 4);      // one arrival per softmax warp
-      mbar_init(bar_o[i], 1);
-      mbar_init(bar_ofree[i], 4);  // one arrival per softmax warp
+      mbar_init(bar_s(i), 1);
+      mbar_init(bar_p(i), 4);      // one arrival per softmax warp
+      mbar_init(bar_o(i), 1);
+      mbar_init(bar_ofree(i), 4);  // one arrival per softmax warp
       mbar_init(smem_u32(&ctl->part_done[i]), 4);
       mbar_init(smem_u32(&ctl->merge_ready[i]), 1);
     }
@@ -551,8 +666,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   // Masked forms: summarise the image ids of every key tile.
-  const int n_all = p.n_tok[0] + p.n_tok[1];
-  TileTable tt{nullptr, nullptr, nullptr};
+  TileTable tt{nullptr};
+  const int* tail_pre = nullptr;
   if constexpr (BC) {
     int* t_lo = reinterpret_cast<int*>(base + C::SUM_OFF);
     int* t_hi = t_lo + MAX_SEQ_TILES;
@@ -561,16 +676,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int lo = 0x7fffffff, hi = -1;
       bool text = false;
       const int pos0 = key_tile_pos(p, t), len = key_tile_len(p, t);
-      for (int e = lane; e < BN; e += 32) {
-        const int j = pos0 + e;
-        if (e < len) {
-          const int id = __ldg(p.image_ids + j);
-          if (id < 0) {
-            text = true;
-          } else {
-            lo = min(lo, id);
-            hi = max(hi, id);
-          }
+      // Lane l summarises keys 4 l .. 4 l + 3 of the tile: one 16-byte load
+      // when the tile is whole and 16-byte aligned (image_ids itself is).
+      int id[4];
+      if (len == BN && (pos0 & 3) == 0) {
+        const int4 v = __ldg(reinterpret_cast<const int4*>(p.image_ids + pos0) + lane);
+        id[0] = v.x;
+        id[1] = v.y;
+        id[2] = v.z;
+        id[3] = v.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          id[e] = (4 * lane + e < len) ? __ldg(p.image_ids + pos0 + 4 * lane + e) : 0;
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (4 * lane + e >= len) continue;  // past the tile's last key
+        if (id[e] < 0) {
+          text = true;
+        } else {
+          lo = min(lo, id[e]);
+          hi = max(hi, id[e]);
         }
       }
       lo = __reduce_min_sync(0xffffffffu, lo);
@@ -582,12 +709,77 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         t_uni[t] = (!text && lo == hi) ? 1 : 0;
       }
     }
-    tt = TileTable{t_lo, t_hi, t_uni};
+    tt = TileTable{t_lo};
+    if (p.sc.tail_ctas > 0) {
+      // Split tail: count the key tiles each tail unit visits (pre[r + 1]),
+      // every (tail unit, key tile) pair to one thread, then turn the counts
+      // into prefix sums (pre[0] = 0).
+      int* pre = reinterpret_cast<int*>(base + C::TAIL_OFF);
+      const int n_tail = p.sc.tail_units;
+      for (int r = threadIdx.x; r <= n_tail; r += NUM_THREADS) pre[r] = 0;
+      __syncthreads();
+      for (int x = threadIdx.x; x < n_tail * T; x += NUM_THREADS) {
+        const int r = x / T, t = x - r * T;
+        if (bc_unit_visits(tt, p, decode_unit(p.sc, true, p.sc.n_whole + r), t))
+          atomicAdd(&pre[r + 1], 1);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        int carry = 0;
+        for (int r0 = 0; r0 < n_tail; r0 += 32) {
+          const int r = r0 + lane;
+          int v = r < n_tail ? pre[r + 1] : 0;
+#pragma unroll
+          for (int d = 1; d < 32; d <<= 1) {
+            const int x = __shfl_up_sync(0xffffffffu, v, d);
+            if (lane >= d) v += x;
+          }
+          if (r < n_tail) pre[r + 1] = carry + v;
+          carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+      }
+      tail_pre = pre;
+      // This CTA's tail items, warp w working out items w, w + 10, ...
+      // (ballots over the key tiles find a unit's v-th visited tile); item j
+      // exists iff items 0 .. j - 1 do, so the count is the first missing one.
+      __syncthreads();
+      if (threadIdx.x == 0) ctl->n_tail_items = MAX_CTA_TAIL_ITEMS;
+      __syncthreads();
+      {
+        Item* items = reinterpret_cast<Item*>(base + C::ITEMS_OFF);
+        auto to_tile = [&](const Unit& u, int v) {
+          int seen = 0;
+          for (int t0 = 0; t0 < T; t0 += 32) {
+            const int t = t0 + lane;
+            unsigned int m = __ballot_sync(0xffffffffu, t < T && bc_unit_visits(tt, p, u, t));
+            const int cnt = __popc(m);
+            if (v < seen + cnt) {
+              for (int skip = v - seen; skip > 0; --skip) m &= m - 1;  // drop lower set bits
+              return t0 + __ffs(m) - 1;
+            }
+            seen += cnt;
+          }
+          return T - 1;
+        };
+        const MaskedTail mt0{&p, tt, pre, nullptr, 0};
+        for (int j = warp; j < MAX_CTA_TAIL_ITEMS; j += NUM_THREADS / 32) {
+          Item it;
+          if (masked_tail_item(p.sc, mt0, T, static_cast<int>(blockIdx.x), j, it, to_tile)) {
+            if (lane == 0) items[j] = it;
+          } else {
+            if (lane == 0) atomicMin(&ctl->n_tail_items, j);
+            break;
+          }
+        }
+      }
+    }
   }
+  MaskedTail mtail{&p, tt, tail_pre, reinterpret_cast<const Item*>(base + C::ITEMS_OFF), 0};
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
+  if (BC && p.sc.tail_ctas > 0) mtail.n_items = ctl->n_tail_items;
   // Loader bookkeeping for draining copies in flight after an abort.
   uint32_t ld_issued = 0, ld_parity = 0;  // per ring slot: a load was issued / its phase
   int q_last = -1;                        // last unit whose Q load was issued
@@ -604,7 +796,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       bool ok = true;
       Item it;
-      for (int n = 0; ok && get_item<BC>(p, T, n, it); ++n) {
+      for (int n = 0; ok && get_item<BC>(p, &mtail, T, n, it); ++n) {
         const Unit& u = it.u;
         // The Q buffers are free once every S MMA of the previous item is done.
         if (n > 0) {
@@ -618,6 +810,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tma_load_4d(qs + i * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tm_q, c * 64, u.h,
                         u.q0 + i * BM, u.b, bar_q);
         q_last = n;
+#pragma unroll 1
         for (int t = it.t_begin; t < it.t_end && ok; ++t) {
           if (BC && !bc_unit_visits(tt, p, u, t)) continue;
           const int seg = (t < T0) ? 0 : 1;
@@ -678,21 +871,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // The first P V of a unit overwrites O_i: wait until the epilogue of the
       // previous unit has read it out of TMEM.
       auto pv = [&](int i, int v_slot, bool accumulate) -> bool {
-        if (!wait_bounded(bar_p[i], (sc[i] - 1u) & 1u, limit, abort_flag, 4)) return false;
+        if (!wait_bounded(bar_p(i), (sc[i] - 1u) & 1u, limit, abort_flag, 4)) return false;
         if (!accumulate && oc[i] > 0 &&
-            !wait_bounded(bar_ofree[i], (oc[i] - 1u) & 1u, limit, abort_flag, 6))
+            !wait_bounded(bar_ofree(i), (oc[i] - 1u) & 1u, limit, abort_flag, 6))
           return false;
         tc_fence_after();
         issue_pv(i, v_slot, accumulate);
         return true;
       };
       Item it;
-      for (int n = 0; ok && get_item<BC>(p, T, n, it); ++n) {
+      for (int n = 0; ok && get_item<BC>(p, &mtail, T, n, it); ++n) {
         const int nq = it.u.two ? 2 : 1;
         ok = wait_bounded(bar_q, n & 1, limit, abort_flag, 2);
         if (!ok) break;
         int v_prev = -1;
         int j = 0;  // key tiles visited so far in this item
+#pragma unroll 1
         for (int t = it.t_begin; t < it.t_end && ok; ++t) {
           if (BC && !bc_unit_visits(tt, p, it.u, t)) continue;
           const int k_slot = slot;
@@ -700,13 +894,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!ok) break;
           if (++slot == C::NSLOT) { slot = 0; phase ^= 1u; }
           tc_fence_after();
-          for (int i = 0; i < nq && ok; ++i) {
+          // Unrolled over the two query tiles, so that sc[] / oc[] are
+          // indexed by constants and stay in registers.
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            if (i >= nq || !ok) break;
             if (j > 0) {
               ok = pv(i, v_prev, j - 1 > 0);
               if (!ok) break;
             }
             issue_s(i, k_slot);
-            mma_commit(bar_s[i]);
+            mma_commit(bar_s(i));
             ++sc[i];
           }
           if (!ok) break;
@@ -721,10 +919,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (!ok) break;
         mma_commit(bar_qfree);  // every S MMA of this item has been issued
-        for (int i = 0; i < nq && ok; ++i) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          if (i >= nq || !ok) break;
           ok = pv(i, v_prev, j - 1 > 0);
           if (!ok) break;
-          mma_commit(bar_o[i]);
+          mma_commit(bar_o(i));
           ++oc[i];
         }
         if (ok) mma_commit(bar_kv_empty(v_prev));
@@ -746,28 +946,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t bar_merge = smem_u32(&ctl->merge_ready[i]);
     const int row = wq * 32 + lane;  // row of the 128-row query tile (= TMEM lane)
     Item it;
-    for (int n = 0; ok && get_item<BC>(p, T, n, it); ++n) {
+    for (int n = 0; ok && get_item<BC>(p, &mtail, T, n, it); ++n) {
       const Unit& u = it.u;
       if (i == 1 && !u.two) continue;
       float m = -INFINITY;  // running (possibly stale) maximum, log2 units
       float l = 0.f;        // running sum of exp2(x - m)
-      RowMask mask{nullptr, nullptr, 0, 0, -1, n_all};
+      RowMask mask{0, 0, -1, u.b, false, false};
       if constexpr (BC) {
         const int qrow = u.q0 + i * BM + row;  // query index; past Nq: a padding row
         mask.qi = p.n_tok[0] + qrow;
         mask.idq = qrow < p.Nq ? __ldg(p.image_ids + mask.qi) : -1;
       }
       int j = 0;  // key tiles visited so far in this item
+#pragma unroll 1
       for (int t = it.t_begin; t < it.t_end; ++t) {
         if constexpr (BC) {
           if (!bc_unit_visits(tt, p, u, t)) continue;
           const bool full = bc_tile_full(tt, p, u.q0 / BM + i, u.q0 + i * BM, t);
           mask.c0 = key_tile_pos(p, t);
-          mask.ids = full ? nullptr : p.image_ids + mask.c0;
-          mask.valid = p.key_valid ? p.key_valid + static_cast<size_t>(u.b) * n_all + mask.c0
-                                   : nullptr;
+          mask.ids = !full;
+          mask.valid = p.key_valid != nullptr;
         }
-        ok = warp_wait(bar_s[i], sc & 1u, limit, abort_flag, 7);
+        ok = warp_wait(bar_s(i), sc & 1u, limit, abort_flag, 7);
         if (!ok) break;
         ++sc;
         tc_fence_after();
@@ -775,15 +975,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // scores must be -inf instead.
         const int seg = (t < T0) ? 0 : 1;
         const int valid = p.n_tok[seg] - (t - (seg ? T0 : 0)) * BN;
-        softmax_tile<D, BC>(s_addr, o_addr, valid, sl2, j > 0, mask, m, l);
+        softmax_tile<D, BC>(s_addr, o_addr, valid, sl2, j > 0, p, mask, m, l);
         ++j;
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_p[i]);
+        if (lane == 0) mbar_arrive(bar_p(i));
       }
       if (!ok) break;
-      ok = warp_wait(bar_o[i], oc & 1u, limit, abort_flag, 8);
+      ok = warp_wait(bar_o(i), oc & 1u, limit, abort_flag, 8);
       if (!ok) break;
       ++oc;
       tc_fence_after();
@@ -794,7 +994,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_ofree[i]);
+      if (lane == 0) mbar_arrive(bar_ofree(i));
 
       const int q = u.q0 + i * BM + row;  // this thread's query row
       uint4* dst = reinterpret_cast<uint4*>(

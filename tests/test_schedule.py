@@ -1,10 +1,11 @@
 """The launch schedule (which CTA runs which unit and key-tile range), computed on
 the host through the library's test hook; no GPU needed.
 
-Every (unit, key tile) pair must be covered exactly once; the pieces of a tail
-unit must partition its key tiles in piece order; workspace slots and arrival
-counters must stay inside what the library allocates (2 x SMs of each); the
-tail must be shared out evenly."""
+Every (unit, key tile) pair must be covered exactly once (masked forms: every
+tile some row of the unit sees, found by brute force over the id vector); the
+pieces of a tail unit must split its tiles in piece order; workspace slots and
+arrival counters must stay inside what the library allocates (2 x SMs of
+each); the tail must be shared out evenly."""
 import collections
 
 import numpy as np
@@ -16,27 +17,44 @@ MAX_PIECES = 8       # pieces one merge reads, plus one for a range boundary
 MIN_PIECE_TILES = 4  # least key tiles per tail CTA
 
 CASES = [
-    # B, Nq, H, key tiles, SMs, masked
-    (1, 4096, 32, 32, 152, False),    # dense N=4096
-    (2, 8192, 32, 64, 152, False),    # dense B=2 N=8192
-    (1, 4096, 32, 40, 152, False),    # prefix 1024 + 4096
-    (1, 32768, 32, 256, 152, False),  # dense N=32768
-    (1, 128, 32, 1, 152, False),      # dense N=128
-    (1, 256, 32, 256, 152, False),    # cross Nq=256, Nk=32768
-    (1, 8192, 32, 4, 152, False),     # cross Nq=8192, Nk=512
-    (1, 1000, 4, 8, 152, False),      # ragged: 16 units on 152 SMs
-    (3, 777, 5, 13, 7, False),
-    (1, 300, 1, 300, 148, False),     # one long unit and a ragged partner
-    (2, 4096, 3, 17, 160, False),
-    (1, 4448, 32, 35, 152, True),     # block-causal: never split
-    (1, 4096, 32, 40, 152, True),     # masked prefix-cached
-    (2, 640, 3, 9, 13, True),
+    # B, Nq, H, key tiles, SMs
+    (1, 4096, 32, 32, 152),    # dense N=4096
+    (2, 8192, 32, 64, 152),    # dense B=2 N=8192
+    (1, 4096, 32, 40, 152),    # prefix 1024 + 4096
+    (1, 32768, 32, 256, 152),  # dense N=32768
+    (1, 128, 32, 1, 152),      # dense N=128
+    (1, 256, 32, 256, 152),    # cross Nq=256, Nk=32768
+    (1, 8192, 32, 4, 152),     # cross Nq=8192, Nk=512
+    (1, 1000, 4, 8, 152),      # ragged: 16 units on 152 SMs
+    (3, 777, 5, 13, 7),
+    (1, 300, 1, 300, 148),     # one long unit and a ragged partner
+    (2, 4096, 3, 17, 160),
+]
+
+# Masked forms: B, Nq, H, Np, id segments over the Np + Nq positions, SMs.
+MASKED = [
+    (1, 4448, 32, 0, ((-1, 333), (0, 2048), (-1, 19), (1, 2048)), 152),  # block-causal
+    (1, 4096, 32, 1024, ((-1, 256), (0, 768), (1, 4096)), 152),          # masked prefix
+    (2, 640, 3, 512, ((-1, 100), (3, 300), (-1, 500), (7, 252)), 13),
+    (1, 3000, 4, 0, ((-1, 3000),), 40),                                   # causal text only
+    (1, 1500, 2, 300, ((5, 1800),), 11),                                  # one image
+    (3, 700, 2, 77, ((-1, 1), (2, 200), (-1, 300), (2, 276)), 9),         # ragged, repeated id
 ]
 
 
-def sched(B, Nq, H, T, sms, masked):
-    rows, grid, slots = ncp.debug_schedule(B, Nq, H, T, sms, masked)
-    return rows, grid, slots
+def masked_ids(Np, Nq, segments):
+    ids = np.concatenate([np.full(n, k, dtype=np.int32) for k, n in segments])
+    assert ids.size == Np + Nq
+    return ids
+
+
+def sched(B, Nq, H, T, sms):
+    return ncp.debug_schedule(B, Nq, H, T, sms, False)
+
+
+def masked_sched(B, Nq, H, Np, segments, sms):
+    ids = masked_ids(Np, Nq, segments)
+    return ncp.debug_schedule(B, Nq, H, 0, sms, True, ids, Np), ids
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -44,9 +62,9 @@ def built():
     ncp.build(quiet=True)
 
 
-@pytest.mark.parametrize("B,Nq,H,T,sms,masked", CASES)
-def test_schedule_covers_every_unit_tile_once(B, Nq, H, T, sms, masked):
-    rows, grid, slots = sched(B, Nq, H, T, sms, masked)
+@pytest.mark.parametrize("B,Nq,H,T,sms", CASES)
+def test_schedule_covers_every_unit_tile_once(B, Nq, H, T, sms):
+    rows, grid, slots = sched(B, Nq, H, T, sms)
     q_pairs = -(-Nq // 256)
     n_units = B * H * q_pairs
     assert 1 <= grid <= sms
@@ -60,9 +78,39 @@ def test_schedule_covers_every_unit_tile_once(B, Nq, H, T, sms, masked):
     assert (seen == 1).all()
 
 
-@pytest.mark.parametrize("B,Nq,H,T,sms,masked", CASES)
-def test_items_are_numbered_per_cta(B, Nq, H, T, sms, masked):
-    rows, grid, _ = sched(B, Nq, H, T, sms, masked)
+def needed_tiles(ids, Np, Nq, q0):
+    """Key tiles (prefix tiles, then current ones) that some query row of the
+    unit at q0 sees, by brute force over every (row, key) pair."""
+    T0, T1 = -(-Np // 128), -(-Nq // 128)
+    pos = np.arange(Np + Nq)
+    rows = np.arange(q0, min(q0 + 256, Nq)) + Np
+    vis = (pos[None, :] <= rows[:, None]) | (
+        (ids[None, pos] >= 0) & (ids[None, pos] == ids[rows][:, None]))
+    key_tile = np.where(pos < Np, pos // 128, T0 + (pos - Np) // 128)
+    need = np.zeros(T0 + T1, dtype=bool)
+    need[np.unique(key_tile[vis.any(axis=0)])] = True
+    return need
+
+
+@pytest.mark.parametrize("B,Nq,H,Np,segments,sms", MASKED)
+def test_masked_schedule_covers_every_needed_tile_once(B, Nq, H, Np, segments, sms):
+    (rows, grid, slots), ids = masked_sched(B, Nq, H, Np, segments, sms)
+    T = -(-Np // 128) + -(-Nq // 128)
+    q_pairs = -(-Nq // 256)
+    assert 1 <= grid <= sms
+    cover = collections.defaultdict(lambda: np.zeros(T, dtype=np.int32))
+    for cta, n, b, h, q0, two, tb, te, tail, piece, pieces, slot0 in rows:
+        assert 0 <= cta < grid and 0 <= b < B and 0 <= h < H and q0 % 256 == 0 and q0 < Nq
+        assert 0 <= tb < te <= T
+        cover[(b, h, q0)][tb:te] += 1
+    assert len(cover) == B * H * q_pairs
+    for (b, h, q0), c in cover.items():
+        need = needed_tiles(ids, Np, Nq, q0)
+        assert (c[need] == 1).all(), (b, h, q0)
+        assert c.max() <= 1  # item ranges of one unit never overlap
+
+
+def check_items_numbered(rows):
     per_cta = collections.defaultdict(list)
     for r in rows:
         per_cta[int(r[0])].append(int(r[1]))
@@ -70,42 +118,65 @@ def test_items_are_numbered_per_cta(B, Nq, H, T, sms, masked):
         assert ns == list(range(len(ns)))
 
 
-@pytest.mark.parametrize("B,Nq,H,T,sms,masked", CASES)
-def test_tail_pieces_partition_their_unit(B, Nq, H, T, sms, masked):
-    rows, grid, slots = sched(B, Nq, H, T, sms, masked)
+def check_tail(rows, grid, slots, T, sms):
     tail = rows[rows[:, 8] >= 0]
     whole = rows[rows[:, 8] < 0]
-    assert (whole[:, 6] == 0).all() and (whole[:, 7] == T).all() and (whole[:, 10] == 1).all()
-    if masked:
-        assert len(tail) == 0
-        return
+    assert (whole[:, 10] == 1).all()
     assert slots <= 2 * sms - 1  # the library allocates 2 x SMs slots
     used_slots = set()
     by_unit = collections.defaultdict(list)
     for r in tail:
         by_unit[int(r[8])].append(r)
-    assert sorted(by_unit) == list(range(len(by_unit)))
-    assert 2 * len(by_unit) <= 2 * sms  # arrival counters
+    assert 2 * len(by_unit) <= 2 * sms  # arrival counters (2 per tail unit)
     for t_unit, items in by_unit.items():
         items.sort(key=lambda r: r[9])
         pieces = int(items[0][10])
-        assert 2 <= pieces <= MAX_PIECES + 1
+        assert pieces >= 2
         assert [int(r[9]) for r in items] == list(range(pieces))
         assert len({(int(r[2]), int(r[3]), int(r[4])) for r in items}) == 1
         assert len({int(r[11]) for r in items}) == 1
-        assert items[0][6] == 0 and items[-1][7] == T
         for a, b in zip(items, items[1:]):
-            assert a[7] == b[6]  # contiguous, in piece order
+            assert a[7] <= b[6]  # disjoint, in piece order
             assert b[0] == a[0] + 1  # consecutive CTAs
         for r in items:
             slot = int(r[11]) + int(r[9])
-            assert 0 <= slot < slots and slot not in used_slots
+            assert 0 <= slot < max(slots, 1) and slot not in used_slots
             used_slots.add(slot)
 
 
-@pytest.mark.parametrize("B,Nq,H,T,sms,masked", CASES)
-def test_work_is_balanced(B, Nq, H, T, sms, masked):
-    rows, grid, _ = sched(B, Nq, H, T, sms, masked)
+@pytest.mark.parametrize("B,Nq,H,T,sms", CASES)
+def test_items_are_numbered_per_cta(B, Nq, H, T, sms):
+    check_items_numbered(sched(B, Nq, H, T, sms)[0])
+
+
+@pytest.mark.parametrize("B,Nq,H,Np,segments,sms", MASKED)
+def test_masked_items_are_numbered_per_cta(B, Nq, H, Np, segments, sms):
+    check_items_numbered(masked_sched(B, Nq, H, Np, segments, sms)[0][0])
+
+
+@pytest.mark.parametrize("B,Nq,H,T,sms", CASES)
+def test_tail_pieces_partition_their_unit(B, Nq, H, T, sms):
+    rows, grid, slots = sched(B, Nq, H, T, sms)
+    check_tail(rows, grid, slots, T, sms)
+    whole = rows[rows[:, 8] < 0]
+    assert (whole[:, 6] == 0).all() and (whole[:, 7] == T).all()
+    tail = rows[rows[:, 8] >= 0]
+    for t_unit in set(tail[:, 8].tolist()):
+        items = sorted(tail[tail[:, 8] == t_unit].tolist(), key=lambda r: r[9])
+        assert items[0][6] == 0 and items[-1][7] == T
+        assert all(a[7] == b[6] for a, b in zip(items, items[1:]))  # contiguous
+
+
+@pytest.mark.parametrize("B,Nq,H,Np,segments,sms", MASKED)
+def test_masked_tail_pieces(B, Nq, H, Np, segments, sms):
+    (rows, grid, slots), _ = masked_sched(B, Nq, H, Np, segments, sms)
+    T = -(-Np // 128) + -(-Nq // 128)
+    check_tail(rows, grid, slots, T, sms)
+
+
+@pytest.mark.parametrize("B,Nq,H,T,sms", CASES)
+def test_work_is_balanced(B, Nq, H, T, sms):
+    rows, grid, _ = sched(B, Nq, H, T, sms)
     q_pairs = -(-Nq // 256)
     n_units = B * H * q_pairs
     work = np.zeros(grid, dtype=np.int64)
@@ -113,7 +184,7 @@ def test_work_is_balanced(B, Nq, H, T, sms, masked):
         work[r[0]] += r[7] - r[6]
     rounds = n_units // sms
     rem = n_units % sms
-    if masked or rem == 0:
+    if rem == 0:
         assert work.max() == T * -(-n_units // grid)
         return
     tail_ctas = min(sms, rem * T // MIN_PIECE_TILES, rem * MAX_PIECES)
@@ -127,12 +198,28 @@ def test_work_is_balanced(B, Nq, H, T, sms, masked):
     assert share.max() == -(-(rem * T) // tail_ctas)
 
 
+def test_masked_prefix_tail_is_shared_out():
+    """Masked prefix workload (every unit visits all 40 tiles): 512 units on
+    152 SMs leave 56 for the last round; their tiles go to every SM."""
+    (rows, grid, slots), _ = masked_sched(1, 4096, 32, 1024, ((-1, 256), (0, 768), (1, 4096)), 152)
+    work = np.zeros(grid, dtype=np.int64)
+    for r in rows:
+        work[r[0]] += r[7] - r[6]
+    assert grid == 152
+    assert work.max() - work.min() <= 1
+    assert work.max() == -(-(512 * 40) // 152)
+
+
 def test_masked_forms_deal_a_snake():
-    B, Nq, H, T, sms = 1, 4448, 32, 35, 152
-    rows, grid, _ = sched(B, Nq, H, T, sms, True)
+    B, Nq, H, Np, seg, sms = MASKED[0]
+    (rows, grid, _), _ = masked_sched(B, Nq, H, Np, seg, sms)
     q_pairs = -(-Nq // 256)
     n_bh = B * H
+    n_units = n_bh * q_pairs
+    whole_rounds = n_units // grid
     for cta, n, b, h, q0, *_ in rows:
+        if n >= whole_rounds:
+            continue
         unit = n * grid + (grid - 1 - cta if n % 2 else cta)
         # longest first: last query pair over all heads, then the one before
         assert q0 // 256 == q_pairs - 1 - unit // n_bh
