@@ -19,7 +19,15 @@
  *   Memory:     all tensor pointers are DEVICE pointers owned by the caller on
  *               the current CUDA device.  Inputs are read only; `out` is fully
  *               overwritten and must not overlap any input.  The library
- *               allocates no device memory per call.
+ *               allocates no device memory per call.  When the work does not
+ *               fill the last round of SMs, the tail is cut into key-range
+ *               pieces on separate SMs whose partial results are merged
+ *               through a split workspace: 2 x SMs slots of 2 x 128 x
+ *               (128 + 4) floats plus 2 x SMs counters (about 40 MB on a
+ *               152-SM GPU), allocated by the first call that splits on each
+ *               (device, stream) pair and kept until the process exits.  A
+ *               call made while its stream is being captured into a CUDA graph
+ *               before that pair has a workspace runs unsplit instead.
  *   Alignment:  every pointer must be 16-byte aligned (tensor-memory-access
  *               descriptors require it).
  *   Head dim:   D must be 64 or 128; H >= 1 (the definitions fix H = 32, any
@@ -71,7 +79,7 @@ int attn_dense_fwd(const void *q, const void *k, const void *v, void *out,
  *   out:  [B, Nq, H, D] bf16, device, written.
  * Nq, Nk >= 1.  When the (b, h, 256-query) work units are fewer than the
  * SMs, each unit's keys are cut into pieces on separate SMs and merged (the
- * split workspace, see attn_prefix_fwd), so short-query, long-context calls
+ * split workspace, see "Memory" above), so short-query, long-context calls
  * still fill the GPU.  Returns ATTN_OK or a negative attn_status.
  */
 int attn_dense_cross_fwd(const void *q, const void *k, const void *v, void *out,
@@ -145,10 +153,11 @@ int attn_masked_prefix_fwd(const void *q, const void *kc, const void *vc, const 
  *
  * Same arguments, result and errors as attn_dense_fwd.  The split workspace
  * (partial rows of key-range pieces and their arrival counters) lives in one
- * static device array of 21.6 MB (160 pieces at D <= 128) that every GPU
- * loading this library holds until the process exits; no cudaMalloc, no
- * cudaFree.  A call whose schedule needs more pieces than that (only on a GPU
- * with more than 160 SMs) returns ATTN_ERR_SHAPE and launches nothing.
+ * static device array of 43.3 MB (320 slots and 320 counters, enough for a
+ * GPU with up to 160 SMs at D <= 128) that every GPU loading this library
+ * holds until the process exits; no cudaMalloc, no cudaFree.  A call whose
+ * schedule needs more than that (only on a GPU with more than 160 SMs)
+ * returns ATTN_ERR_SHAPE and launches nothing.
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress); make that first call before any stream capture.
  * Every call clears the counters on `stream`, then uses the array: calls
