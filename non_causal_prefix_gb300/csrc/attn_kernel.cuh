@@ -384,23 +384,20 @@ struct RowMask {
   bool valid;  // test key_valid (false: every key valid)
 };
 
-// One 128-key tile of the online softmax for this thread's query row:
-// S (fp32, TMEM) -> running max m and sum l (log2 domain) -> P (bf16) written
-// over the first 64 columns of S; O is rescaled in TMEM when m moved.
-template <int D, bool BC>
-__device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, int valid, float sl2,
-                                             bool may_rescale, const Params& p,
-                                             const RowMask& mask, float& m, float& l) {
+// Masked forms: this row's visibility of one key tile's 128 keys as a
+// bitmask (masked: some key is hidden).  It reads only the image ids and
+// key_valid, so the softmax warps build it while they wait for the tile's
+// scores.
+__device__ __forceinline__ void build_row_mask(const Params& p, const RowMask& mask,
+                                               uint32_t (&vis)[4], bool& masked) {
   const int n_keys = p.n_tok[0] + p.n_tok[1];  // key positions (nothing past them is read)
-  // Masked forms: this row's visibility of the tile's 128 keys as a bitmask,
-  // built before the scores are loaded so that fewer registers are live.  The
-  // warp builds it together (the flags are warp-uniform): lane l reads the
+  // The warp builds it together (the flags are warp-uniform): lane l reads the
   // ids and flags of keys l, 32 + l, 64 + l, 96 + l (coalesced), so that one
   // ballot per 32 keys gives a mask word in key order.
-  uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
-  bool masked = false;
+  vis[0] = vis[1] = vis[2] = vis[3] = ~0u;
+  masked = false;
   const int lane = static_cast<int>(threadIdx.x & 31u);
-  if (BC && mask.ids) {
+  if (mask.ids) {
     masked = true;
     const int* ids = p.image_ids + mask.c0;
     int kid[4];  // keys past the last position read as text; `valid` masks them
@@ -429,7 +426,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, i
       pending &= ~__ballot_sync(0xffffffffu, mine);
     }
   }
-  if (BC && mask.valid) {
+  if (mask.valid) {
     // key_valid, the same for every row: keys past the last position count
     // as valid here (`valid` masks them).
     const unsigned char* kv = p.key_valid + static_cast<size_t>(mask.b) * n_keys + mask.c0;
@@ -447,6 +444,15 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, i
       for (int e = 0; e < 4; ++e) vis[e] &= okw[e];
     }
   }
+}
+
+// One 128-key tile of the online softmax for this thread's query row:
+// S (fp32, TMEM) -> running max m and sum l (log2 domain) -> P (bf16) written
+// over the first 64 columns of S; O is rescaled in TMEM when m moved.
+template <int D, bool BC>
+__device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, int valid, float sl2,
+                                             bool may_rescale, const uint32_t (&vis)[4],
+                                             bool masked, float& m, float& l) {
   float s[BN];
   {
     uint32_t r[BN];
@@ -967,6 +973,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mask.ids = !full;
           mask.valid = p.key_valid != nullptr;
         }
+        uint32_t vis[4] = {~0u, ~0u, ~0u, ~0u};
+        bool masked = false;
+        if constexpr (BC) build_row_mask(p, mask, vis, masked);
         ok = warp_wait(bar_s(i), sc & 1u, limit, abort_flag, 7);
         if (!ok) break;
         ++sc;
@@ -975,7 +984,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // scores must be -inf instead.
         const int seg = (t < T0) ? 0 : 1;
         const int valid = p.n_tok[seg] - (t - (seg ? T0 : 0)) * BN;
-        softmax_tile<D, BC>(s_addr, o_addr, valid, sl2, j > 0, p, mask, m, l);
+        softmax_tile<D, BC>(s_addr, o_addr, valid, sl2, j > 0, vis, masked, m, l);
         ++j;
         tmem_wait_st();
         tc_fence_before();
