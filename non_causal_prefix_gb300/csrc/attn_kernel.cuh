@@ -83,6 +83,7 @@ struct SharedCtl {
   uint64_t part_done[2];   // the 4 warps of a query tile wrote their partial rows
   uint64_t merge_ready[2]; // the piece's arrival count is known (SharedCtl::last)
   uint64_t drain;
+  uint64_t tail_ready;     // masked forms: this CTA's tail items are in shared memory
   int last[2];             // this piece is the last of its unit: merge and store
   int n_tail_items;        // masked forms: tail items of this CTA kept in shared memory
   uint32_t tmem_base;
@@ -660,6 +661,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(smem_u32(&ctl->merge_ready[i]), 1);
     }
     mbar_init(smem_u32(&ctl->drain), 1);
+    mbar_init(smem_u32(&ctl->tail_ready), 1);
+    ctl->n_tail_items = MAX_CTA_TAIL_ITEMS;
     ctl->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -671,121 +674,80 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // Masked forms: summarise the image ids of every key tile.
+  // Masked forms: summarise the image ids of every key tile (the roles' tile
+  // walk needs it from their first item on).  Each warp takes 4 tiles at a
+  // time with their loads in flight together; lane l summarises keys
+  // 4 l .. 4 l + 3 of a tile, with one 16-byte load when the tile is whole and
+  // 16-byte aligned (image_ids itself is).
   TileTable tt{nullptr};
-  const int* tail_pre = nullptr;
   if constexpr (BC) {
+    constexpr int NW = NUM_THREADS / 32;
     int* t_lo = reinterpret_cast<int*>(base + C::SUM_OFF);
-    int* t_hi = t_lo + MAX_SEQ_TILES;
-    int* t_uni = t_hi + MAX_SEQ_TILES;
-    for (int t = warp; t < T; t += NUM_THREADS / 32) {
-      int lo = 0x7fffffff, hi = -1;
-      bool text = false;
-      const int pos0 = key_tile_pos(p, t), len = key_tile_len(p, t);
-      // Lane l summarises keys 4 l .. 4 l + 3 of the tile: one 16-byte load
-      // when the tile is whole and 16-byte aligned (image_ids itself is).
-      int id[4];
-      if (len == BN && (pos0 & 3) == 0) {
-        const int4 v = __ldg(reinterpret_cast<const int4*>(p.image_ids + pos0) + lane);
-        id[0] = v.x;
-        id[1] = v.y;
-        id[2] = v.z;
-        id[3] = v.w;
-      } else {
+    for (int t0 = warp; t0 < T; t0 += 4 * NW) {
+      int id[4][4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          id[e] = (4 * lane + e < len) ? __ldg(p.image_ids + pos0 + 4 * lane + e) : 0;
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (4 * lane + e >= len) continue;  // past the tile's last key
-        if (id[e] < 0) {
-          text = true;
+      for (int b = 0; b < 4; ++b) {
+        const int t = t0 + b * NW;
+        if (t >= T) continue;
+        const int pos0 = key_tile_pos(p, t), len = key_tile_len(p, t);
+        if (len == BN && (pos0 & 3) == 0) {
+          const int4 v = __ldg(reinterpret_cast<const int4*>(p.image_ids + pos0) + lane);
+          id[b][0] = v.x;
+          id[b][1] = v.y;
+          id[b][2] = v.z;
+          id[b][3] = v.w;
         } else {
-          lo = min(lo, id[e]);
-          hi = max(hi, id[e]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            id[b][e] = (4 * lane + e < len) ? __ldg(p.image_ids + pos0 + 4 * lane + e) : 0;
         }
       }
-      lo = __reduce_min_sync(0xffffffffu, lo);
-      hi = __reduce_max_sync(0xffffffffu, hi);
-      text = __any_sync(0xffffffffu, text);
-      if (lane == 0) {
-        t_lo[t] = lo;
-        t_hi[t] = hi;
-        t_uni[t] = (!text && lo == hi) ? 1 : 0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int t = t0 + b * NW;
+        if (t >= T) continue;  // warp-uniform
+        const int len = key_tile_len(p, t);
+        int lo = 0x7fffffff, hi = -1;
+        bool text = false;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (4 * lane + e >= len) continue;  // past the tile's last key
+          if (id[b][e] < 0) {
+            text = true;
+          } else {
+            lo = min(lo, id[b][e]);
+            hi = max(hi, id[b][e]);
+          }
+        }
+        lo = __reduce_min_sync(0xffffffffu, lo);
+        hi = __reduce_max_sync(0xffffffffu, hi);
+        text = __any_sync(0xffffffffu, text);
+        if (lane == 0) {
+          t_lo[t] = lo;
+          t_lo[MAX_SEQ_TILES + t] = hi;
+          t_lo[2 * MAX_SEQ_TILES + t] = (!text && lo == hi) ? 1 : 0;
+        }
       }
     }
     tt = TileTable{t_lo};
-    if (p.sc.tail_ctas > 0) {
-      // Split tail: count the key tiles each tail unit visits (pre[r + 1]),
-      // every (tail unit, key tile) pair to one thread, then turn the counts
-      // into prefix sums (pre[0] = 0).
-      int* pre = reinterpret_cast<int*>(base + C::TAIL_OFF);
-      const int n_tail = p.sc.tail_units;
-      for (int r = threadIdx.x; r <= n_tail; r += NUM_THREADS) pre[r] = 0;
-      __syncthreads();
-      for (int x = threadIdx.x; x < n_tail * T; x += NUM_THREADS) {
-        const int r = x / T, t = x - r * T;
-        if (bc_unit_visits(tt, p, decode_unit(p.sc, true, p.sc.n_whole + r), t))
-          atomicAdd(&pre[r + 1], 1);
-      }
-      __syncthreads();
-      if (warp == 0) {
-        int carry = 0;
-        for (int r0 = 0; r0 < n_tail; r0 += 32) {
-          const int r = r0 + lane;
-          int v = r < n_tail ? pre[r + 1] : 0;
-#pragma unroll
-          for (int d = 1; d < 32; d <<= 1) {
-            const int x = __shfl_up_sync(0xffffffffu, v, d);
-            if (lane >= d) v += x;
-          }
-          if (r < n_tail) pre[r + 1] = carry + v;
-          carry += __shfl_sync(0xffffffffu, v, 31);
-        }
-      }
-      tail_pre = pre;
-      // This CTA's tail items, warp w working out items w, w + 10, ...
-      // (ballots over the key tiles find a unit's v-th visited tile); item j
-      // exists iff items 0 .. j - 1 do, so the count is the first missing one.
-      __syncthreads();
-      if (threadIdx.x == 0) ctl->n_tail_items = MAX_CTA_TAIL_ITEMS;
-      __syncthreads();
-      {
-        Item* items = reinterpret_cast<Item*>(base + C::ITEMS_OFF);
-        auto to_tile = [&](const Unit& u, int v) {
-          int seen = 0;
-          for (int t0 = 0; t0 < T; t0 += 32) {
-            const int t = t0 + lane;
-            unsigned int m = __ballot_sync(0xffffffffu, t < T && bc_unit_visits(tt, p, u, t));
-            const int cnt = __popc(m);
-            if (v < seen + cnt) {
-              for (int skip = v - seen; skip > 0; --skip) m &= m - 1;  // drop lower set bits
-              return t0 + __ffs(m) - 1;
-            }
-            seen += cnt;
-          }
-          return T - 1;
-        };
-        const MaskedTail mt0{&p, tt, pre, nullptr, 0};
-        for (int j = warp; j < MAX_CTA_TAIL_ITEMS; j += NUM_THREADS / 32) {
-          Item it;
-          if (masked_tail_item(p.sc, mt0, T, static_cast<int>(blockIdx.x), j, it, to_tile)) {
-            if (lane == 0) items[j] = it;
-          } else {
-            if (lane == 0) atomicMin(&ctl->n_tail_items, j);
-            break;
-          }
-        }
-      }
-    }
   }
+  const bool masked_tail = BC && p.sc.tail_ctas > 0;
+  const int* tail_pre = masked_tail ? reinterpret_cast<const int*>(base + C::TAIL_OFF) : nullptr;
   MaskedTail mtail{&p, tt, tail_pre, reinterpret_cast<const Item*>(base + C::ITEMS_OFF), 0};
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  if (BC && p.sc.tail_ctas > 0) mtail.n_items = ctl->n_tail_items;
+  // Masked forms with a split tail: the first tail item of a CTA's loader and
+  // MMA issuer waits until the softmax warps have worked the tail items out.
+  const int tail_rounds = p.sc.tail_ctas ? p.sc.n_whole / static_cast<int>(gridDim.x) : 0;
+  const uint32_t bar_tail = smem_u32(&ctl->tail_ready);
+  auto await_tail = [&](int n, int site) -> bool {
+    if (!masked_tail || n < tail_rounds || mtail.n_items > 0) return true;
+    if (!wait_bounded(bar_tail, 0, limit, abort_flag, site)) return false;
+    mtail.n_items = ctl->n_tail_items;
+    return true;
+  };
   // Loader bookkeeping for draining copies in flight after an abort.
   uint32_t ld_issued = 0, ld_parity = 0;  // per ring slot: a load was issued / its phase
   int q_last = -1;                        // last unit whose Q load was issued
@@ -802,7 +764,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       bool ok = true;
       Item it;
-      for (int n = 0; ok && get_item<BC>(p, &mtail, T, n, it); ++n) {
+      for (int n = 0; ok && (ok = await_tail(n, 12)) && get_item<BC>(p, &mtail, T, n, it); ++n) {
         const Unit& u = it.u;
         // The Q buffers are free once every S MMA of the previous item is done.
         if (n > 0) {
@@ -886,7 +848,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         return true;
       };
       Item it;
-      for (int n = 0; ok && get_item<BC>(p, &mtail, T, n, it); ++n) {
+      for (int n = 0; ok && (ok = await_tail(n, 13)) && get_item<BC>(p, &mtail, T, n, it); ++n) {
         const int nq = it.u.two ? 2 : 1;
         ok = wait_bounded(bar_q, n & 1, limit, abort_flag, 2);
         if (!ok) break;
@@ -951,6 +913,72 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t bar_part = smem_u32(&ctl->part_done[i]);
     const uint32_t bar_merge = smem_u32(&ctl->merge_ready[i]);
     const int row = wq * 32 + lane;  // row of the 128-row query tile (= TMEM lane)
+    if (masked_tail) {
+      // The split tail's schedule, worked out by the 8 softmax warps (named
+      // barrier 1, before any bounded wait of theirs) while the loader and the
+      // MMA issuer start on the whole units: the visited tiles of each tail
+      // unit (one (unit, tile) pair per thread, shared-memory atomics), their
+      // prefix sums (warp 0, shuffles), then this CTA's tail items, warp w
+      // taking items w, w + 8, ... (ballots over a unit's key tiles find its
+      // v-th visited tile).  Item j exists iff items 0 .. j - 1 do, so the
+      // count is the first missing one.
+      constexpr int NS = 8 * 32;
+      int* pre = reinterpret_cast<int*>(base + C::TAIL_OFF);
+      const int n_tail = p.sc.tail_units;
+      for (int r = threadIdx.x; r <= n_tail; r += NS) pre[r] = 0;
+      named_barrier(1, NS);
+      for (int x = threadIdx.x; x < n_tail * T; x += NS) {
+        const int r = x / T, t = x - r * T;
+        if (bc_unit_visits(tt, p, decode_unit(p.sc, true, p.sc.n_whole + r), t))
+          atomicAdd(&pre[r + 1], 1);
+      }
+      named_barrier(1, NS);
+      if (warp == 0) {
+        int carry = 0;
+        for (int r0 = 0; r0 < n_tail; r0 += 32) {
+          const int r = r0 + lane;
+          int v = r < n_tail ? pre[r + 1] : 0;
+#pragma unroll
+          for (int d = 1; d < 32; d <<= 1) {
+            const int x = __shfl_up_sync(0xffffffffu, v, d);
+            if (lane >= d) v += x;
+          }
+          if (r < n_tail) pre[r + 1] = carry + v;
+          carry += __shfl_sync(0xffffffffu, v, 31);
+        }
+      }
+      named_barrier(1, NS);
+      {
+        Item* items = reinterpret_cast<Item*>(base + C::ITEMS_OFF);
+        auto to_tile = [&](const Unit& uu, int v) {
+          int seen = 0;
+          for (int t0 = 0; t0 < T; t0 += 32) {
+            const int t = t0 + lane;
+            unsigned int msk = __ballot_sync(0xffffffffu, t < T && bc_unit_visits(tt, p, uu, t));
+            const int cnt = __popc(msk);
+            if (v < seen + cnt) {
+              for (int skip = v - seen; skip > 0; --skip) msk &= msk - 1;  // drop lower set bits
+              return t0 + __ffs(msk) - 1;
+            }
+            seen += cnt;
+          }
+          return T - 1;
+        };
+        const MaskedTail mt0{&p, tt, pre, nullptr, 0};
+        for (int jj = warp; jj < MAX_CTA_TAIL_ITEMS; jj += 8) {
+          Item ti;
+          if (masked_tail_item(p.sc, mt0, T, static_cast<int>(blockIdx.x), jj, ti, to_tile)) {
+            if (lane == 0) items[jj] = ti;
+          } else {
+            if (lane == 0) atomicMin(&ctl->n_tail_items, jj);
+            break;
+          }
+        }
+      }
+      named_barrier(1, NS);
+      if (threadIdx.x == 0) mbar_arrive(bar_tail);
+      mtail.n_items = ctl->n_tail_items;
+    }
     Item it;
     for (int n = 0; ok && get_item<BC>(p, &mtail, T, n, it); ++n) {
       const Unit& u = it.u;
