@@ -65,3 +65,21 @@ def build(force: bool = False, quiet: bool = False, extra_flags=None) -> str:
         print(res.stderr.strip())
     os.replace(tmp, LIB_PATH)
     return LIB_PATH
+
+
+def build_variant(name: str, extra_flags) -> str:
+    """Build the same sources with extra compile flags into
+    ``_lib/libncp_attn_<name>.so`` (test builds that exercise rare paths);
+    rebuilt when missing or stale."""
+    path = os.path.join(LIB_DIR, f"libncp_attn_{name}.so")
+    if os.path.exists(path) and all(os.path.getmtime(f) <= os.path.getmtime(path)
+                                    for f in _inputs()):
+        return path
+    os.makedirs(LIB_DIR, exist_ok=True)
+    tmp = path + f".tmp{os.getpid()}"
+    cmd = [nvcc(), *NVCC_FLAGS, *extra_flags, "-I", INCLUDE, "-o", tmp, *sources()]
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + res.stdout + res.stderr)
+    os.replace(tmp, path)
+    return path

@@ -245,8 +245,12 @@ struct MaskedTail {
 };
 
 // Most tail items of one CTA kept in shared memory (later ones, rare, are
-// worked out when reached).
-constexpr int MAX_CTA_TAIL_ITEMS = 32;
+// worked out when reached).  Overridable with -D to test that path.
+#ifndef NCP_MAX_CTA_TAIL_ITEMS
+#define NCP_MAX_CTA_TAIL_ITEMS 32
+#endif
+constexpr int MAX_CTA_TAIL_ITEMS = NCP_MAX_CTA_TAIL_ITEMS;
+static_assert(MAX_CTA_TAIL_ITEMS >= 1 && MAX_CTA_TAIL_ITEMS <= 32, "tail item list: 1 to 32 items");
 static_assert(sizeof(Item) <= 48, "tail item list: 48 bytes per item in shared memory");
 
 // CTAs sharing a masked tail of W visited tiles: at most the launch's
