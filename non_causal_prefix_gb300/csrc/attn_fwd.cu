@@ -22,6 +22,7 @@
 
 #include <cmath>
 #include <map>
+#include <algorithm>
 #include <mutex>
 #include <vector>
 #include <utility>
@@ -112,7 +113,37 @@ bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) !
 // visit a data-dependent subset of each unit's key tiles: T bounds their
 // work here, and the kernel shares out the tail by the tiles actually
 // visited.  Returns the grid size.
-int make_sched(ncp::Sched& s, long long n_units, int T, int sms, bool can_split) {
+// Cost of one extra tail piece on a CTA, in key-tile times: its Q load and
+// pipeline fill, its partial written and counted in, and the merge.
+// Measured on GB300: a CTA with two tail pieces ends about 6 tiles after one
+// with a single piece of the same length.
+constexpr long long PIECE_COST = 5;
+
+// Dense tail ranges: cut W tail tiles (units of T tiles, in order) into
+// consecutive non-empty ranges, each CTA's tiles plus PIECE_COST for every
+// unit boundary it crosses at most `cap`; a CTA only crosses into the next
+// unit with budget left for a tile there.  Returns the number of ranges
+// (bounds[0 .. n]), or -1 if more than g are needed.
+int tail_ranges(long long W, long long T, long long g, long long cap, int* bounds) {
+  long long pos = 0;
+  int n = 0;
+  bounds[0] = 0;
+  while (pos < W) {
+    if (n >= g) return -1;
+    long long budget = cap;
+    while (true) {
+      const long long take = std::min(T - pos % T, std::min(budget, W - pos));
+      pos += take;
+      budget -= take;
+      if (pos >= W || budget <= PIECE_COST || pos % T != 0) break;
+      budget -= PIECE_COST;  // cross into the next unit
+    }
+    bounds[++n] = static_cast<int>(pos);
+  }
+  return n;
+}
+
+int make_sched(ncp::Sched& s, long long n_units, int T, int sms, bool can_split, bool masked) {
   s.n_units = static_cast<int>(n_units);
   s.n_whole = s.n_units;
   s.tail_units = 0;
@@ -123,10 +154,21 @@ int make_sched(ncp::Sched& s, long long n_units, int T, int sms, bool can_split)
     long long g_tail = sms;
     if (g_tail > W / ncp::MIN_PIECE_TILES) g_tail = W / ncp::MIN_PIECE_TILES;
     if (g_tail > rem * ncp::MAX_PIECES) g_tail = rem * ncp::MAX_PIECES;
+    if (!masked && g_tail > ncp::MAX_TAIL_CTAS) g_tail = ncp::MAX_TAIL_CTAS;
     if (g_tail > rem && rem <= ncp::MAX_TAIL_UNITS) {
       s.n_whole = static_cast<int>(n_units - rem);
       s.tail_units = static_cast<int>(rem);
       s.tail_ctas = static_cast<int>(g_tail);
+      if (!masked) {
+        // The least per-CTA cost whose ranges fit in g_tail CTAs (binary
+        // search; one CTA taking everything always fits).
+        long long lo = (W + g_tail - 1) / g_tail, hi = W + PIECE_COST * rem;
+        while (lo < hi) {
+          const long long mid = (lo + hi) / 2;
+          if (tail_ranges(W, T, g_tail, mid, s.bounds) >= 0) hi = mid; else lo = mid + 1;
+        }
+        s.tail_ctas = tail_ranges(W, T, g_tail, lo, s.bounds);
+      }
       return s.n_whole > 0 ? sms : s.tail_ctas;
     }
   }
@@ -217,11 +259,11 @@ int launch(Params& prm, long long n_units, cudaStream_t stream) {
   int dev = 0, sms = 0;
   if (configure<D, BC>(&dev, &sms) != ATTN_OK) return ATTN_ERR_CUDA;
   const int T = prm.n_tiles[0] + prm.n_tiles[1];
-  int grid = make_sched(prm.sc, n_units, T, sms, true);
+  int grid = make_sched(prm.sc, n_units, T, sms, true, BC);
   const Workspace* ws = nullptr;
   if (prm.sc.tail_ctas > 0) {
     ws = get_workspace(dev, sms, stream);
-    if (!ws) grid = make_sched(prm.sc, n_units, T, sms, false);
+    if (!ws) grid = make_sched(prm.sc, n_units, T, sms, false, BC);
   }
   prm.ws_part = ws ? ws->part : nullptr;
   prm.ws_count = ws ? ws->count : nullptr;
@@ -317,7 +359,7 @@ int launch_noalloc(Params& prm, long long n_units, cudaStream_t stream) {
   int dev = 0, sms = 0;
   if (configure<D, false>(&dev, &sms) != ATTN_OK) return ATTN_ERR_CUDA;
   const int T = prm.n_tiles[0] + prm.n_tiles[1];
-  const int grid = make_sched(prm.sc, n_units, T, sms, true);
+  const int grid = make_sched(prm.sc, n_units, T, sms, true, false);
   if (sched_slots(prm.sc) > ncp::NOALLOC_SLOTS || 2 * prm.sc.tail_units > ncp::NOALLOC_COUNTERS)
     return ATTN_ERR_SHAPE;
   void* scratch = nullptr;
@@ -474,7 +516,7 @@ int attn_debug_schedule(int B, int Nq, int H, int n_key_tiles, int sms, int mask
   s.q_pairs = static_cast<int>(q_pairs);
   s.H = H;
   s.Nq = Nq;
-  const int grid = make_sched(s, n_units, T, sms, true);
+  const int grid = make_sched(s, n_units, T, sms, true, masked != 0);
   // Masked forms: the kernel's tile table and tail prefix sums, built here.
   std::vector<int> table(3 * ncp::MAX_SEQ_TILES, 0), pre(s.tail_units + 1, 0);
   ncp::MaskedTail mt{&prm, ncp::TileTable{table.data()}, pre.data()};

@@ -28,6 +28,9 @@ constexpr int MAX_SEQ_TILES = 1024;
 constexpr int MAX_PIECES = 8;
 constexpr int MIN_PIECE_TILES = 4;
 constexpr int MAX_TAIL_UNITS = 1024;
+// Dense forms: most CTAs sharing a tail (their range bounds travel in the
+// kernel parameters).
+constexpr int MAX_TAIL_CTAS = 256;
 // Rescale O only when the running row maximum (log2 units) grows by more than
 // this; otherwise keep the stale maximum.  Exact, because the final 1/l uses
 // the same maximum as the accumulated O, and p <= 2^8 stays far from overflow.
@@ -99,6 +102,9 @@ struct Sched {
   int n_whole;     // units walked whole
   int tail_units;  // units after them, cut into key ranges (0: none)
   int tail_ctas;   // CTAs sharing the tail (0: no tail)
+  // Dense forms: CTA c of the tail holds tail tiles [bounds[c], bounds[c + 1])
+  // (tiles of the tail units in unit order), every range non-empty.
+  int bounds[MAX_TAIL_CTAS + 1];
 };
 
 struct Params {
@@ -262,16 +268,16 @@ __host__ __device__ __forceinline__ long long masked_tail_ctas(const Sched& s, l
 }
 
 // Fill `it` with the tail piece of tail unit r that covers tail positions
-// [lo, hi) clipped to the unit's [u0, u1), positions held by CTAs of G over
-// W; `base`: the unit's first position.  to_tile maps a position inside the
-// unit to its key tile (identity for the dense forms).
-template <class ToTile>
+// [lo, hi) clipped to the unit's [u0, u1); owner(x) is the CTA holding tail
+// position x.  to_tile maps a position inside the unit to its key tile
+// (identity for the dense forms).
+template <class Owner, class ToTile>
 __host__ __device__ __forceinline__ void tail_piece(const Sched& s, bool bc, int c, long long r,
                                                     long long lo, long long hi, long long u0,
-                                                    long long u1, long long W, long long G,
-                                                    ToTile to_tile, Item& it) {
-  const long long first = tail_owner(u0, W, G);
-  const long long last = tail_owner(u1 - 1, W, G);
+                                                    long long u1, Owner owner, ToTile to_tile,
+                                                    Item& it) {
+  const long long first = owner(u0);
+  const long long last = owner(u1 - 1);
   const int v0 = static_cast<int>((lo > u0 ? lo : u0) - u0);
   const int v1 = static_cast<int>((hi < u1 ? hi : u1) - u0);
   it.u = decode_unit(s, bc, s.n_whole + static_cast<int>(r));
@@ -310,7 +316,8 @@ __host__ __device__ __forceinline__ bool masked_tail_item(const Sched& s, const 
   }
   const int r = a + j;
   if (r >= s.tail_units || pre[r] >= hi) return false;
-  tail_piece(s, true, c, r, lo, hi, pre[r], pre[r + 1], W, G, to_tile, it);
+  tail_piece(s, true, c, r, lo, hi, pre[r], pre[r + 1],
+             [&](long long x) { return tail_owner(x, W, G); }, to_tile, it);
   return true;
 }
 
@@ -322,8 +329,9 @@ __host__ __device__ __forceinline__ bool masked_tail_item(const Sched& s, const 
 //
 // Tail: the n_whole = rounds * g first units go the same way; the work of the
 // tail_units units left is laid out in unit order as W tail positions and cut
-// into G equal ranges, one per CTA c < G.  Dense forms: a position is a key
-// tile, W = tail_units * T, G = tail_ctas.  Masked forms: a position is a
+// into G ranges, one per CTA c < G.  Dense forms: a position is a key tile,
+// W = tail_units * T, and the ranges (s.bounds, chosen on the host) weigh each
+// extra piece a CTA takes.  Masked forms (equal ranges): a position is a
 // *visited* key tile (mt->pre counts them), G = masked_tail_ctas(W).  A range
 // that crosses a unit boundary gives its CTA one piece of each unit.  Each
 // piece leaves its partial (O, m, l) in workspace slot c + r (r: the tail
@@ -346,12 +354,20 @@ __host__ __device__ __forceinline__ bool schedule_item(const Sched& s, int T, in
   }
   const int j = n - rounds;  // tail item of this CTA
   if (!BC) {
-    const long long W = static_cast<long long>(s.tail_units) * T, G = s.tail_ctas;
+    const int G = s.tail_ctas;
     if (c >= G) return false;
-    const long long lo = c * W / G, hi = (c + 1) * W / G;
+    const long long lo = s.bounds[c], hi = s.bounds[c + 1];
     const long long r = lo / T + j;
     if (r >= s.tail_units || r * T >= hi) return false;
-    tail_piece(s, false, c, r, lo, hi, r * T, (r + 1) * T, W, G,
+    auto owner = [&](long long x) {  // the last CTA whose range starts at or before x
+      int a = 0, b = G - 1;
+      while (a < b) {
+        const int mid = (a + b + 1) / 2;
+        if (s.bounds[mid] <= x) a = mid; else b = mid - 1;
+      }
+      return static_cast<long long>(a);
+    };
+    tail_piece(s, false, c, r, lo, hi, r * T, (r + 1) * T, owner,
                [](const Unit&, int v) { return v; }, it);
     return true;
   }

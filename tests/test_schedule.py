@@ -174,6 +174,30 @@ def test_masked_tail_pieces(B, Nq, H, Np, segments, sms):
     check_tail(rows, grid, slots, T, sms)
 
 
+PIECE_COST = 5  # the library's cost of an extra tail piece on a CTA, in key-tile times
+
+
+def cta_costs(rows, T):
+    """Per tail CTA: its tail tiles plus PIECE_COST for each tail item after
+    its first."""
+    tail = rows[rows[:, 8] >= 0]
+    costs = {}
+    for c in set(tail[:, 0].tolist()):
+        mine = tail[tail[:, 0] == c]
+        costs[c] = int((mine[:, 7] - mine[:, 6]).sum()) + PIECE_COST * (len(mine) - 1)
+    return costs
+
+
+def equal_range_cost(W, T, G):
+    """The largest per-CTA cost of G equal ranges over W tail tiles."""
+    worst = 0
+    for c in range(G):
+        lo, hi = c * W // G, (c + 1) * W // G
+        if lo < hi:
+            worst = max(worst, hi - lo + PIECE_COST * ((hi - 1) // T - lo // T))
+    return worst
+
+
 @pytest.mark.parametrize("B,Nq,H,T,sms", CASES)
 def test_work_is_balanced(B, Nq, H, T, sms):
     rows, grid, _ = sched(B, Nq, H, T, sms)
@@ -187,15 +211,18 @@ def test_work_is_balanced(B, Nq, H, T, sms):
     if rem == 0:
         assert work.max() == T * -(-n_units // grid)
         return
-    tail_ctas = min(sms, rem * T // MIN_PIECE_TILES, rem * MAX_PIECES)
-    if tail_ctas <= rem:  # not worth splitting: the last round runs whole units
-        assert work.max() == T * (rounds + 1)
+    g_max = min(sms, rem * T // MIN_PIECE_TILES, rem * MAX_PIECES)
+    tail = rows[rows[:, 8] >= 0]
+    if g_max <= rem:  # not worth splitting: the last round runs whole units
+        assert len(tail) == 0 and work.max() == T * (rounds + 1)
         return
-    share = work - rounds * T
-    share = share[share > 0]
-    assert len(share) == tail_ctas
-    assert share.max() - share.min() <= 1
-    assert share.max() == -(-(rem * T) // tail_ctas)
+    costs = cta_costs(rows, T)
+    assert rem < len(costs) <= g_max
+    # Every tail CTA works; the weighted ranges are no worse than equal ones,
+    # and within one piece's cost of each other.
+    assert all(v > 0 for v in costs.values())
+    assert max(costs.values()) <= equal_range_cost(rem * T, T, g_max)
+    assert max(costs.values()) - min(costs.values()) <= PIECE_COST + T
 
 
 def test_masked_prefix_tail_is_shared_out():
