@@ -519,14 +519,25 @@ int attn_debug_schedule(int B, int Nq, int H, int n_key_tiles, int sms, int mask
   const int grid = make_sched(s, n_units, T, sms, true, masked != 0);
   // Masked forms: the kernel's tile table and tail prefix sums, built here.
   std::vector<int> table(3 * ncp::MAX_SEQ_TILES, 0), pre(s.tail_units + 1, 0);
-  ncp::MaskedTail mt{&prm, ncp::TileTable{table.data()}, pre.data()};
+  std::vector<int> order(ncp::ORDER_QP + 2 * ncp::MAX_Q_PAIRS, 0);
+  ncp::MaskedTail mt{&prm, ncp::TileTable{table.data()}, pre.data(), nullptr, 0,
+                     ncp::UnitOrder{order.data()}};
   if (masked) {
     if (!image_ids) return ATTN_ERR_NULL;
+    if (q_pairs > ncp::MAX_Q_PAIRS) return ATTN_ERR_SHAPE;
     for (int t = 0; t < T; ++t)
       ncp::tile_summary(prm, image_ids, t, table[t], table[ncp::MAX_SEQ_TILES + t],
                         table[2 * ncp::MAX_SEQ_TILES + t]);
+    int* cnt = order.data() + ncp::ORDER_QP + ncp::MAX_Q_PAIRS;
+    for (int q = 0; q < s.q_pairs; ++q) {
+      ncp::Unit uq{0, 0, q * 2 * ncp::BM, q * 2 * ncp::BM + ncp::BM < Nq};
+      for (int t = 0; t < T; ++t) cnt[q] += ncp::bc_unit_visits(mt.tt, prm, uq, t) ? 1 : 0;
+    }
+    for (int q = 0; q < s.q_pairs; ++q)
+      order[ncp::ORDER_QP + ncp::order_rank(cnt, s.q_pairs, q)] = q;
+    ncp::order_levels(order.data(), cnt, s.q_pairs);
     for (int r = 0; r < s.tail_units; ++r) {
-      const ncp::Unit u = ncp::decode_unit(s, true, s.n_whole + r);
+      const ncp::Unit u = ncp::decode_unit(s, true, s.n_whole + r, &mt.ord);
       int cnt = 0;
       for (int t = 0; t < T; ++t) cnt += ncp::bc_unit_visits(mt.tt, prm, u, t) ? 1 : 0;
       pre[r + 1] = pre[r] + cnt;

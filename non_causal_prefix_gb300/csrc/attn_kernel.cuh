@@ -31,6 +31,8 @@ constexpr int MAX_TAIL_UNITS = 1024;
 // Dense forms: most CTAs sharing a tail (their range bounds travel in the
 // kernel parameters).
 constexpr int MAX_TAIL_CTAS = 256;
+// Masked forms: most query pairs (256-row units along the sequence).
+constexpr int MAX_Q_PAIRS = MAX_SEQ_TILES / 2;
 // Rescale O only when the running row maximum (log2 units) grows by more than
 // this; otherwise keep the stale maximum.  Exact, because the final 1/l uses
 // the same maximum as the accumulated O, and p <= 2^8 stays far from overflow.
@@ -63,7 +65,8 @@ struct Cfg {
   static constexpr uint32_t SUM_OFF = BAR_OFF + 512;             // masked forms: tile table
   static constexpr uint32_t TAIL_OFF = SUM_OFF + 3 * 4 * MAX_SEQ_TILES;  // and tail prefix sums
   static constexpr uint32_t ITEMS_OFF = TAIL_OFF + 4 * (MAX_TAIL_UNITS + 4);  // and tail items
-  static constexpr uint32_t SMEM_BYTES_BC = ITEMS_OFF + 48 * 32 + 1024;
+  static constexpr uint32_t ORDER_OFF = ITEMS_OFF + 48 * 32;  // and the unit order tables
+  static constexpr uint32_t SMEM_BYTES_BC = ORDER_OFF + 4 * (3 * MAX_Q_PAIRS + 2) + 1024;
   // Share of the exponentials computed by the FMA-pipe polynomial instead of
   // the MUFU unit: POLY_NUM of every POLY_DEN packed pairs.  On GB300 the
   // MUFU unit does about 30 exp2 per clock per SM and the polynomial about 13:
@@ -136,15 +139,60 @@ struct Unit {
   bool two;  // the second 128-row query tile has at least one row
 };
 
-__host__ __device__ __forceinline__ Unit decode_unit(const Sched& s, bool bc, int unit) {
+// Masked forms: the order of the units.  A unit's work is the number of key
+// tiles its query pair visits (the same for every batch and head), so the
+// query pairs are sorted by that count, most first (ties: the later pair
+// first); pairs of one count form a level.  Units go level by level, and
+// within a level head-major with the query pair fastest, as in the dense
+// order, so that the CTAs running at one time share few heads' K/V in L2.
+// Tables (int block): [0] number of levels L, [1 .. L + 1] first index into
+// qp_order of each level (then q_pairs), then qp_order[q_pairs] at
+// ORDER_QP = 2 + MAX_Q_PAIRS.
+struct UnitOrder {
+  const int* tab;
+};
+constexpr int ORDER_QP = 2 + MAX_Q_PAIRS;
+
+// Position of query pair q in the unit order, from the visited-tile counts
+// of the q_pairs pairs: more tiles first, the later pair first among equals.
+__host__ __device__ __forceinline__ int order_rank(const int* cnt, int q_pairs, int q) {
+  int rank = 0;
+  const int cq = cnt[q];
+  for (int q2 = 0; q2 < q_pairs; ++q2) rank += (cnt[q2] > cq || (cnt[q2] == cq && q2 > q)) ? 1 : 0;
+  return rank;
+}
+
+// The levels of the order table `ob` once its qp_order is filled (one thread).
+__host__ __device__ __forceinline__ void order_levels(int* ob, const int* cnt, int q_pairs) {
+  int n_lvl = 0;
+  for (int r = 0; r < q_pairs; ++r)
+    if (r == 0 || cnt[ob[ORDER_QP + r]] != cnt[ob[ORDER_QP + r - 1]]) ob[1 + n_lvl++] = r;
+  ob[1 + n_lvl] = q_pairs;
+  ob[0] = n_lvl;
+}
+
+__host__ __device__ __forceinline__ Unit decode_unit(const Sched& s, bool bc, int unit,
+                                                     const UnitOrder* ord = nullptr) {
   Unit u;
   // Dense forms: query pair fastest, so the CTAs running at one time share
-  // the K/V of a few heads in L2.  Masked forms: rows see more keys the later
-  // they sit, so hand out the last query pairs first, over all heads (longest
-  // work first; all heads' K/V stay in L2 at these lengths).
+  // the K/V of a few heads in L2.  Masked forms: by levels of work (above).
   const int n_bh = s.n_units / s.q_pairs;  // B * H
-  const int qp = bc ? s.q_pairs - 1 - unit / n_bh : unit % s.q_pairs;
-  const int bh = bc ? unit % n_bh : unit / s.q_pairs;
+  int qp, bh;
+  if (bc) {
+    const int* lvl = ord->tab + 1;
+    int a = 0, b = ord->tab[0] - 1;  // the level holding this unit
+    while (a < b) {
+      const int mid = (a + b + 1) / 2;
+      if (lvl[mid] * n_bh <= unit) a = mid; else b = mid - 1;
+    }
+    const int len = lvl[a + 1] - lvl[a];
+    const int w = unit - lvl[a] * n_bh;
+    bh = w / len;
+    qp = ord->tab[ORDER_QP + lvl[a] + w % len];
+  } else {
+    qp = unit % s.q_pairs;
+    bh = unit / s.q_pairs;
+  }
   u.h = bh % s.H;
   u.b = bh / s.H;
   u.q0 = qp * (2 * BM);
@@ -248,6 +296,7 @@ struct MaskedTail {
   const int* pre;
   const Item* items;
   int n_items;
+  UnitOrder ord;
 };
 
 // Most tail items of one CTA kept in shared memory (later ones, rare, are
@@ -275,12 +324,12 @@ template <class Owner, class ToTile>
 __host__ __device__ __forceinline__ void tail_piece(const Sched& s, bool bc, int c, long long r,
                                                     long long lo, long long hi, long long u0,
                                                     long long u1, Owner owner, ToTile to_tile,
-                                                    Item& it) {
+                                                    const UnitOrder* ord, Item& it) {
   const long long first = owner(u0);
   const long long last = owner(u1 - 1);
   const int v0 = static_cast<int>((lo > u0 ? lo : u0) - u0);
   const int v1 = static_cast<int>((hi < u1 ? hi : u1) - u0);
-  it.u = decode_unit(s, bc, s.n_whole + static_cast<int>(r));
+  it.u = decode_unit(s, bc, s.n_whole + static_cast<int>(r), ord);
   it.t_begin = to_tile(it.u, v0);
   it.t_end = to_tile(it.u, v1 - 1) + 1;
   if (first == last) {  // the whole unit in one range: no merge
@@ -317,7 +366,7 @@ __host__ __device__ __forceinline__ bool masked_tail_item(const Sched& s, const 
   const int r = a + j;
   if (r >= s.tail_units || pre[r] >= hi) return false;
   tail_piece(s, true, c, r, lo, hi, pre[r], pre[r + 1],
-             [&](long long x) { return tail_owner(x, W, G); }, to_tile, it);
+             [&](long long x) { return tail_owner(x, W, G); }, to_tile, &mt.ord, it);
   return true;
 }
 
@@ -349,7 +398,7 @@ __host__ __device__ __forceinline__ bool schedule_item(const Sched& s, int T, in
   if (s.tail_ctas == 0 || n < rounds) {
     const int unit = n * g + ((BC && (n & 1)) ? g - 1 - c : c);
     if (unit >= s.n_whole) return false;
-    it.u = decode_unit(s, BC, unit);
+    it.u = decode_unit(s, BC, unit, BC ? &mt->ord : nullptr);
     return true;
   }
   const int j = n - rounds;  // tail item of this CTA
@@ -368,7 +417,7 @@ __host__ __device__ __forceinline__ bool schedule_item(const Sched& s, int T, in
       return static_cast<long long>(a);
     };
     tail_piece(s, false, c, r, lo, hi, r * T, (r + 1) * T, owner,
-               [](const Unit&, int v) { return v; }, it);
+               [](const Unit&, int v) { return v; }, nullptr, it);
     return true;
   }
   return masked_tail_item(s, *mt, T, c, j, it, [&](const Unit& u, int v) {
@@ -750,10 +799,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     tt = TileTable{t_lo};
+    // The unit order (see UnitOrder): visited tiles per query pair, then
+    // each pair's rank, then the levels.
+    int* ob = reinterpret_cast<int*>(base + C::ORDER_OFF);
+    int* cnt = ob + ORDER_QP + MAX_Q_PAIRS;
+    const int qpn = p.sc.q_pairs;
+    for (int q = threadIdx.x; q < qpn; q += NUM_THREADS) cnt[q] = 0;
+    __syncthreads();
+    for (int x = threadIdx.x; x < qpn * T; x += NUM_THREADS) {
+      const int q = x / T, t = x - q * T;
+      Unit uq;
+      uq.b = 0;
+      uq.h = 0;
+      uq.q0 = q * 2 * BM;
+      uq.two = uq.q0 + BM < p.Nq;
+      if (bc_unit_visits(tt, p, uq, t)) atomicAdd(&cnt[q], 1);
+    }
+    __syncthreads();
+    for (int q = threadIdx.x; q < qpn; q += NUM_THREADS) ob[ORDER_QP + order_rank(cnt, qpn, q)] = q;
+    __syncthreads();
+    if (threadIdx.x == 0) order_levels(ob, cnt, qpn);
   }
   const bool masked_tail = BC && p.sc.tail_ctas > 0;
   const int* tail_pre = masked_tail ? reinterpret_cast<const int*>(base + C::TAIL_OFF) : nullptr;
-  MaskedTail mtail{&p, tt, tail_pre, reinterpret_cast<const Item*>(base + C::ITEMS_OFF), 0};
+  MaskedTail mtail{&p, tt, tail_pre, reinterpret_cast<const Item*>(base + C::ITEMS_OFF), 0,
+                   UnitOrder{BC ? reinterpret_cast<const int*>(base + C::ORDER_OFF) : nullptr}};
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -949,7 +1019,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       named_barrier(1, NS);
       for (int x = threadIdx.x; x < n_tail * T; x += NS) {
         const int r = x / T, t = x - r * T;
-        if (bc_unit_visits(tt, p, decode_unit(p.sc, true, p.sc.n_whole + r), t))
+        if (bc_unit_visits(tt, p, decode_unit(p.sc, true, p.sc.n_whole + r, &mtail.ord), t))
           atomicAdd(&pre[r + 1], 1);
       }
       named_barrier(1, NS);
@@ -984,7 +1054,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           return T - 1;
         };
-        const MaskedTail mt0{&p, tt, pre, nullptr, 0};
+        const MaskedTail mt0{&p, tt, pre, nullptr, 0, mtail.ord};
         for (int jj = warp; jj < MAX_CTA_TAIL_ITEMS; jj += 8) {
           Item ti;
           if (masked_tail_item(p.sc, mt0, T, static_cast<int>(blockIdx.x), jj, ti, to_tile)) {

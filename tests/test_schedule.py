@@ -237,17 +237,54 @@ def test_masked_prefix_tail_is_shared_out():
     assert work.max() == -(-(512 * 40) // 152)
 
 
-def test_masked_forms_deal_a_snake():
-    B, Nq, H, Np, seg, sms = MASKED[0]
-    (rows, grid, _), _ = masked_sched(B, Nq, H, Np, seg, sms)
-    q_pairs = -(-Nq // 256)
+def visited_per_pair(ids, Np, Nq):
+    """Key tiles each query pair's unit visits (the kernel's skip rule, restated:
+    a tile is visited when it starts at or before the pair's last row, or when
+    its image ids' range meets the pair's)."""
+    T0, T1 = -(-Np // 128), -(-Nq // 128)
+    pos0 = [t * 128 if t < T0 else Np + (t - T0) * 128 for t in range(T0 + T1)]
+    ln = [min(128, (Np if t < T0 else Nq) - (t if t < T0 else t - T0) * 128) for t in range(T0 + T1)]
+    lo, hi = [], []
+    for t in range(T0 + T1):
+        seg = ids[pos0[t]:pos0[t] + ln[t]]
+        img = seg[seg >= 0]
+        lo.append(int(img.min()) if img.size else 2**31 - 1)
+        hi.append(int(img.max()) if img.size else -1)
+    counts = []
+    for q in range(-(-Nq // 256)):
+        r_last = Np + min(q * 256 + 256, Nq) - 1
+        qt0 = T0 + 2 * q
+        qt1 = qt0 + 1 if q * 256 + 128 < Nq else qt0
+        qlo, qhi = min(lo[qt0], lo[qt1]), max(hi[qt0], hi[qt1])
+        counts.append(sum(1 for t in range(T0 + T1)
+                          if pos0[t] <= r_last or (qlo <= hi[t] and lo[t] <= qhi)))
+    return counts
+
+
+@pytest.mark.parametrize("B,Nq,H,Np,segments,sms", MASKED)
+def test_masked_forms_deal_a_snake(B, Nq, H, Np, segments, sms):
+    """Whole masked units: query pairs sorted by the key tiles they visit (most
+    first, the later pair first among equals); units level by level, head-major
+    with the query pair fastest within a level; dealt in a snake."""
+    (rows, grid, _), ids = masked_sched(B, Nq, H, Np, segments, sms)
+    cnt = visited_per_pair(ids, Np, Nq)
+    q_pairs = len(cnt)
     n_bh = B * H
-    n_units = n_bh * q_pairs
-    whole_rounds = n_units // grid
+    order = sorted(range(q_pairs), key=lambda q: (-cnt[q], -q))
+    levels = [r for r in range(q_pairs) if r == 0 or cnt[order[r]] != cnt[order[r - 1]]]
+    levels.append(q_pairs)
+    whole_rounds = (n_bh * q_pairs) // grid
     for cta, n, b, h, q0, *_ in rows:
         if n >= whole_rounds:
             continue
         unit = n * grid + (grid - 1 - cta if n % 2 else cta)
-        # longest first: last query pair over all heads, then the one before
-        assert q0 // 256 == q_pairs - 1 - unit // n_bh
-        assert b * H + h == unit % n_bh
+        lv = max(i for i in range(len(levels) - 1) if levels[i] * n_bh <= unit)
+        size = levels[lv + 1] - levels[lv]
+        w = unit - levels[lv] * n_bh
+        assert b * H + h == w // size
+        assert q0 // 256 == order[levels[lv] + w % size]
+    # Units of whole rounds come in non-increasing work.
+    units = sorted((n * grid + (grid - 1 - cta if n % 2 else cta), q0 // 256)
+                   for cta, n, b, h, q0, *_ in rows if n < whole_rounds)
+    work = [cnt[q] for _, q in units]
+    assert all(a >= b for a, b in zip(work, work[1:]))
