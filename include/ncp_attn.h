@@ -27,7 +27,11 @@
  *               152-SM GPU), allocated by the first call that splits on each
  *               (device, stream) pair and kept until the process exits.  A
  *               call made while its stream is being captured into a CUDA graph
- *               before that pair has a workspace runs unsplit instead.
+ *               before that pair has a workspace runs unsplit instead.  A
+ *               graph captured after that keeps the capture stream's
+ *               workspace: its replays must not run at the same time as other
+ *               work using that workspace (calls on the capture stream, or
+ *               replays of other graphs captured on it).
  *   Alignment:  every pointer must be 16-byte aligned (tensor-memory-access
  *               descriptors require it).
  *   Head dim:   D must be 64 or 128; H >= 1 (the definitions fix H = 32, any
