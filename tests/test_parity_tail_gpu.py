@@ -90,3 +90,34 @@ def test_split_tail_rows(cuda_lib, oracle_mod, case):
     torch.cuda.synchronize()
     got = out.float().cpu().numpy().astype(np.float64).reshape(-1, D)[rows]
     assert_parity(got, ref, f"{kind} B={B} Nq={Nq} Np={Np} Nk={Nk} H={H} D={D} (split tail rows)")
+
+
+def test_masked_split_tail_deterministic_and_per_stream(cuda_lib):
+    """A block-causal call whose tail is split: repeated calls are
+    bit-identical, and calls on two streams at once (separate workspaces)
+    agree with them."""
+    B, N, H, D = 1, 2000, 20, 64
+    segs = ((-1, 100), (2, 1900))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ids = torch.cat([torch.full((n,), k, dtype=torch.int32) for k, n in segs])
+    sched, _, _ = cuda_lib.debug_schedule(B, N, H, 0, sms, True, ids.numpy(), 0)
+    if not (sched[:, 8] >= 0).any():
+        pytest.skip(f"no split tail with {sms} SMs")
+    q, k, v = (workloads.randn_bf16((B, N, H, D), 1.0, 19500 + i).cuda() for i in range(3))
+    dids = ids.cuda()
+    first = torch.empty_like(q)
+    cuda_lib.attn_block_causal_fwd(q, k, v, dids, first)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        again = torch.empty_like(q)
+        cuda_lib.attn_block_causal_fwd(q, k, v, dids, again)
+        torch.cuda.synchronize()
+        assert torch.equal(again, first)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [torch.empty_like(q) for _ in streams]
+    for _ in range(4):
+        for s, o in zip(streams, outs):
+            cuda_lib.attn_block_causal_fwd(q, k, v, dids, o, stream=s)
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(o, first)
