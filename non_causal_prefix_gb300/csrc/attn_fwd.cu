@@ -114,10 +114,11 @@ bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) !
 // work here, and the kernel shares out the tail by the tiles actually
 // visited.  Returns the grid size.
 // Cost of one extra tail piece on a CTA, in key-tile times: its Q load and
-// pipeline fill, its partial written and counted in, and the merge.
-// Measured on GB300: a CTA with two tail pieces ends about 6 tiles after one
-// with a single piece of the same length.
-constexpr long long PIECE_COST = 5;
+// pipeline fill, its partial written and counted in, and the merge.  On
+// GB300 a CTA with two tail pieces ends about 6 tiles after one with a single
+// piece of the same length, but part of that overlaps; of the costs 1, 2, 3,
+// 5 and 8 tried, 3 gave the shortest launches.
+constexpr long long PIECE_COST = 3;
 
 // Dense tail ranges: cut W tail tiles (units of T tiles, in order) into
 // consecutive non-empty ranges, each CTA's tiles plus PIECE_COST for every

@@ -174,7 +174,7 @@ def test_masked_tail_pieces(B, Nq, H, Np, segments, sms):
     check_tail(rows, grid, slots, T, sms)
 
 
-PIECE_COST = 5  # the library's cost of an extra tail piece on a CTA, in key-tile times
+PIECE_COST = 3  # the library's cost of an extra tail piece on a CTA, in key-tile times
 
 
 def cta_costs(rows, T):
