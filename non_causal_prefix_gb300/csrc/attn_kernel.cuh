@@ -308,6 +308,17 @@ constexpr int MAX_CTA_TAIL_ITEMS = NCP_MAX_CTA_TAIL_ITEMS;
 static_assert(MAX_CTA_TAIL_ITEMS >= 1 && MAX_CTA_TAIL_ITEMS <= 32, "tail item list: 1 to 32 items");
 static_assert(sizeof(Item) <= 48, "tail item list: 48 bytes per item in shared memory");
 
+// Masked forms' tail: the cost of one tail item, in visited key tiles, over
+// and above its tiles (a Q load, a pipeline fill and an epilogue; for a piece
+// also the partial write and count-in).  Charged once per tail unit, at the
+// unit's start: a CTA whose range takes in many small units, or crosses into
+// a second unit, gets correspondingly fewer tiles.  Overridable with -D.
+#ifndef NCP_MASKED_UNIT_COST
+#define NCP_MASKED_UNIT_COST 3
+#endif
+constexpr int MASKED_UNIT_COST = NCP_MASKED_UNIT_COST;
+static_assert(MASKED_UNIT_COST >= 0, "masked tail unit cost");
+
 // CTAs sharing a masked tail of W visited tiles: at most the launch's
 // tail_ctas, and at least MIN_PIECE_TILES visited tiles each.
 __host__ __device__ __forceinline__ long long masked_tail_ctas(const Sched& s, long long W) {
@@ -351,21 +362,28 @@ template <class ToTile>
 __host__ __device__ __forceinline__ bool masked_tail_item(const Sched& s, const MaskedTail& mt,
                                                           int T, int c, int j, Item& it,
                                                           ToTile to_tile) {
-  const int* pre = mt.pre;
-  const long long W = pre[s.tail_units], G = masked_tail_ctas(s, W);
+  // Cost positions: tail unit r spans [P(r), P(r + 1)), MASKED_UNIT_COST
+  // positions of item cost and then its visited tiles.
+  constexpr long long UC = MASKED_UNIT_COST;
+  auto P = [&](int r) { return static_cast<long long>(mt.pre[r]) + UC * r; };
+  const long long G = masked_tail_ctas(s, mt.pre[s.tail_units]);
+  const long long W = P(s.tail_units);
   if (c >= G) return false;
   const long long lo = c * W / G, hi = (c + 1) * W / G;
   if (lo >= hi) return false;
-  // The tail unit holding position lo: the last r with pre[r] <= lo (pre
-  // rises strictly: every unit visits its diagonal tiles).
+  // The tail unit holding position lo: the last r with P(r) <= lo (P rises
+  // strictly: every unit visits its diagonal tiles).
   int a = 0, b = s.tail_units - 1;
   while (a < b) {
     const int mid = (a + b + 1) / 2;
-    if (pre[mid] <= lo) a = mid; else b = mid - 1;
+    if (P(mid) <= lo) a = mid; else b = mid - 1;
   }
+  // Item j: the j-th unit whose tiles meet [lo, hi).  Past the first, every
+  // unit the range reaches does (its tiles follow its cost positions); the
+  // first may be missed only when the range ends inside its cost positions.
   const int r = a + j;
-  if (r >= s.tail_units || pre[r] >= hi) return false;
-  tail_piece(s, true, c, r, lo, hi, pre[r], pre[r + 1],
+  if (r >= s.tail_units || P(r) + UC >= hi) return false;
+  tail_piece(s, true, c, r, lo, hi, P(r) + UC, P(r + 1),
              [&](long long x) { return tail_owner(x, W, G); }, to_tile, &mt.ord, it);
   return true;
 }
@@ -380,8 +398,9 @@ __host__ __device__ __forceinline__ bool masked_tail_item(const Sched& s, const 
 // tail_units units left is laid out in unit order as W tail positions and cut
 // into G ranges, one per CTA c < G.  Dense forms: a position is a key tile,
 // W = tail_units * T, and the ranges (s.bounds, chosen on the host) weigh each
-// extra piece a CTA takes.  Masked forms (equal ranges): a position is a
-// *visited* key tile (mt->pre counts them), G = masked_tail_ctas(W).  A range
+// extra piece a CTA takes.  Masked forms (equal ranges of cost): each unit is
+// MASKED_UNIT_COST positions of item cost, then one position per *visited*
+// key tile (mt->pre counts them), G = masked_tail_ctas(visited tiles).  A range
 // that crosses a unit boundary gives its CTA one piece of each unit.  Each
 // piece leaves its partial (O, m, l) in workspace slot c + r (r: the tail
 // unit), which is unique: a CTA later in the order only meets later units.

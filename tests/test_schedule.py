@@ -15,6 +15,7 @@ import non_causal_prefix_gb300 as ncp
 
 MAX_PIECES = 8       # pieces one merge reads, plus one for a range boundary
 MIN_PIECE_TILES = 4  # least key tiles per tail CTA
+UNIT_COST = 3        # masked tails: item cost per tail unit, in visited key tiles
 
 CASES = [
     # B, Nq, H, key tiles, SMs
@@ -227,14 +228,42 @@ def test_work_is_balanced(B, Nq, H, T, sms):
 
 def test_masked_prefix_tail_is_shared_out():
     """Masked prefix workload (every unit visits all 40 tiles): 512 units on
-    152 SMs leave 56 for the last round; their tiles go to every SM."""
+    152 SMs leave 56 for the last round; their tiles go to every SM, and a CTA
+    whose range crosses into a second unit (two tail items) pays that unit's
+    UNIT_COST: it holds that many fewer tiles than the fullest one-item CTA."""
     (rows, grid, slots), _ = masked_sched(1, 4096, 32, 1024, ((-1, 256), (0, 768), (1, 4096)), 152)
-    work = np.zeros(grid, dtype=np.int64)
-    for r in rows:
-        work[r[0]] += r[7] - r[6]
     assert grid == 152
-    assert work.max() - work.min() <= 1
-    assert work.max() == -(-(512 * 40) // 152)
+    rounds = 512 // 152
+    tiles = np.zeros(grid, dtype=np.int64)
+    items = np.zeros(grid, dtype=np.int64)
+    for r in rows:
+        if r[1] >= rounds:
+            tiles[r[0]] += r[7] - r[6]
+            items[r[0]] += 1
+    assert tiles.sum() == 56 * 40 and (items >= 1).all()
+    per_cta = 56 * (40 + UNIT_COST) / 152
+    cost = tiles + UNIT_COST * (items - 1)
+    assert cost.max() <= np.ceil(per_cta) and cost.min() >= np.floor(per_cta) - UNIT_COST
+    assert tiles[items == 2].max() + UNIT_COST <= tiles[items == 1].max() + 1
+
+
+def visited_tiles(ids, Np, Nq, q):
+    """Key tiles the unit of query pair q visits, in order (the kernel's skip
+    rule, as in visited_per_pair)."""
+    T0, T1 = -(-Np // 128), -(-Nq // 128)
+    pos0 = [t * 128 if t < T0 else Np + (t - T0) * 128 for t in range(T0 + T1)]
+    ln = [min(128, (Np if t < T0 else Nq) - (t if t < T0 else t - T0) * 128) for t in range(T0 + T1)]
+    lo, hi = [], []
+    for t in range(T0 + T1):
+        seg = ids[pos0[t]:pos0[t] + ln[t]]
+        img = seg[seg >= 0]
+        lo.append(int(img.min()) if img.size else 2**31 - 1)
+        hi.append(int(img.max()) if img.size else -1)
+    r_last = Np + min(q * 256 + 256, Nq) - 1
+    qt0 = T0 + 2 * q
+    qt1 = qt0 + 1 if q * 256 + 128 < Nq else qt0
+    qlo, qhi = min(lo[qt0], lo[qt1]), max(hi[qt0], hi[qt1])
+    return [t for t in range(T0 + T1) if pos0[t] <= r_last or (qlo <= hi[t] and lo[t] <= qhi)]
 
 
 def visited_per_pair(ids, Np, Nq):
@@ -288,3 +317,53 @@ def test_masked_forms_deal_a_snake(B, Nq, H, Np, segments, sms):
                    for cta, n, b, h, q0, *_ in rows if n < whole_rounds)
     work = [cnt[q] for _, q in units]
     assert all(a >= b for a, b in zip(work, work[1:]))
+
+
+@pytest.mark.parametrize("B,Nq,H,Np,segments,sms", MASKED)
+def test_masked_tail_layout(B, Nq, H, Np, segments, sms):
+    """The masked tail, restated: tail units in unit order, each worth
+    UNIT_COST positions and then one per visited key tile; CTA c of G holds
+    positions [c W / G, (c + 1) W / G) and one item per unit whose tiles meet
+    that range, with the visited tiles that fall in it."""
+    (rows, grid, _), ids = masked_sched(B, Nq, H, Np, segments, sms)
+    cnt = visited_per_pair(ids, Np, Nq)
+    q_pairs, n_bh = len(cnt), B * H
+    n_units = n_bh * q_pairs
+    rem = n_units % grid if grid == sms else 0
+    T = -(-Np // 128) + -(-Nq // 128)
+    g_tail = min(sms, rem * T // MIN_PIECE_TILES, rem * MAX_PIECES)
+    tail_rows = [r for r in rows if r[1] >= n_units // grid] if rem and g_tail > rem else []
+    if not tail_rows:
+        return
+    order = sorted(range(q_pairs), key=lambda q: (-cnt[q], -q))
+    levels = [r for r in range(q_pairs) if r == 0 or cnt[order[r]] != cnt[order[r - 1]]]
+    levels.append(q_pairs)
+
+    def unit_pair(u):
+        lv = max(i for i in range(len(levels) - 1) if levels[i] * n_bh <= u)
+        size = levels[lv + 1] - levels[lv]
+        w = u - levels[lv] * n_bh
+        return w // size, order[levels[lv] + w % size]
+
+    tail = [unit_pair(u) for u in range(n_units - rem, n_units)]
+    vis = [cnt[q] for _, q in tail]
+    pos = np.concatenate([[0], np.cumsum(np.array(vis) + UNIT_COST)])
+    W, G = int(pos[-1]), max(1, min(sum(vis) // MIN_PIECE_TILES, g_tail))
+    expect = collections.defaultdict(list)
+    for c in range(G):
+        lo, hi = c * W // G, (c + 1) * W // G
+        for r, (bh, q) in enumerate(tail):
+            u0, u1 = pos[r] + UNIT_COST, pos[r + 1]
+            if max(lo, u0) < min(hi, u1):
+                expect[c].append((bh, q, max(lo, u0) - u0, min(hi, u1) - u0))
+    # Visited tiles of a pair, in order (the kernel's skip rule), to turn an
+    # item's tile range into visited indices.
+    T0 = -(-Np // 128)
+    got = collections.defaultdict(list)
+    for cta, n, b, h, q0, two, tb, te, *_ in sorted(tail_rows, key=lambda r: (r[0], r[1])):
+        q = q0 // 256
+        seen = visited_tiles(ids, Np, Nq, q)
+        v0 = seen.index(tb)
+        v1 = seen.index(te - 1) + 1
+        got[cta].append((b * H + h, q, v0, v1))
+    assert dict(got) == dict(expect)
