@@ -362,12 +362,13 @@ template <class ToTile>
 __host__ __device__ __forceinline__ bool masked_tail_item(const Sched& s, const MaskedTail& mt,
                                                           int T, int c, int j, Item& it,
                                                           ToTile to_tile) {
-  // Cost positions: tail unit r spans [P(r), P(r + 1)), MASKED_UNIT_COST
-  // positions of item cost and then its visited tiles.
-  constexpr long long UC = MASKED_UNIT_COST;
-  auto P = [&](int r) { return static_cast<long long>(mt.pre[r]) + UC * r; };
-  const long long G = masked_tail_ctas(s, mt.pre[s.tail_units]);
-  const long long W = P(s.tail_units);
+  // Cost positions: tail unit r spans [P(r), P(r + 1)), P(r) = pre[r] + C r
+  // with C = MASKED_UNIT_COST: C positions of item cost, then its visited
+  // tiles.
+  constexpr int C = MASKED_UNIT_COST;
+  const int* pre = mt.pre;
+  const long long G = masked_tail_ctas(s, pre[s.tail_units]);
+  const long long W = pre[s.tail_units] + static_cast<long long>(C) * s.tail_units;
   if (c >= G) return false;
   const long long lo = c * W / G, hi = (c + 1) * W / G;
   if (lo >= hi) return false;
@@ -376,14 +377,14 @@ __host__ __device__ __forceinline__ bool masked_tail_item(const Sched& s, const 
   int a = 0, b = s.tail_units - 1;
   while (a < b) {
     const int mid = (a + b + 1) / 2;
-    if (P(mid) <= lo) a = mid; else b = mid - 1;
+    if (pre[mid] + C * mid <= lo) a = mid; else b = mid - 1;
   }
   // Item j: the j-th unit whose tiles meet [lo, hi).  Past the first, every
   // unit the range reaches does (its tiles follow its cost positions); the
   // first may be missed only when the range ends inside its cost positions.
   const int r = a + j;
-  if (r >= s.tail_units || P(r) + UC >= hi) return false;
-  tail_piece(s, true, c, r, lo, hi, P(r) + UC, P(r + 1),
+  if (r >= s.tail_units || pre[r] + C * (r + 1) >= hi) return false;
+  tail_piece(s, true, c, r, lo, hi, pre[r] + C * (r + 1), pre[r + 1] + C * (r + 1),
              [&](long long x) { return tail_owner(x, W, G); }, to_tile, &mt.ord, it);
   return true;
 }
