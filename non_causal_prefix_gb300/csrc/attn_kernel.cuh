@@ -646,10 +646,13 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, i
 // apart).  Pieces are combined in piece order, so the result does not depend
 // on which piece finished last: the common maximum and the sum first, then O
 // in groups of 64 columns (16 loads in flight per piece), stored as bf16 to
-// `dst` (nullptr: a padding row, nothing stored).  Kept out of line so that
-// its registers do not weigh on the softmax loop's allocation.
-template <int D>
-__device__ __noinline__ void merge_pieces(const float4* part, int nk, uint4* dst) {
+// `dst` (nullptr: a padding row, nothing stored).  With OWN, the merging piece
+// `own` takes its O from TMEM (this row's lane at o_taddr), where it still
+// is, instead of reading back its partial: the same values, 1 / nk fewer
+// bytes (called by whole warps then: the TMEM loads are warp-wide).
+template <int D, bool OWN>
+__device__ __forceinline__ void merge_rows(const float4* part, int nk, uint4* dst, int own,
+                                           uint32_t o_taddr) {
   constexpr int NG = D / 4 + 1;
   const size_t piece_stride = static_cast<size_t>(2) * NG * BM;
   float m_all = -INFINITY;
@@ -669,68 +672,7 @@ __device__ __noinline__ void merge_pieces(const float4* part, int nk, uint4* dst
     for (int k = 0; k < nk; ++k) {
       const float4* src = part + k * piece_stride;
       float4 v[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) v[e] = __ldcg(src + (cg * 16 + e) * BM);
-      const float a = ex2(__ldcg(src + (D / 4) * BM).x - m_all);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        acc[4 * e] = fmaf(v[e].x, a, acc[4 * e]);
-        acc[4 * e + 1] = fmaf(v[e].y, a, acc[4 * e + 1]);
-        acc[4 * e + 2] = fmaf(v[e].z, a, acc[4 * e + 2]);
-        acc[4 * e + 3] = fmaf(v[e].w, a, acc[4 * e + 3]);
-      }
-    }
-    if (dst) {
-#pragma unroll
-      for (int c = 0; c < 64; c += 8) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float o0, o1;
-          up2(fmul2(pk2(acc[c + 2 * e], acc[c + 2 * e + 1]), inv2), o0, o1);
-          w[e] = pack_bf16x2(o0, o1);
-        }
-        dst[(cg * 64 + c) / 8] = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-    }
-  }
-}
-
-// merge_pieces for D = 64, where the merging piece takes its own O from
-// TMEM.  Merge of a tail unit's pieces for one row: `part` points at this row's
-// partial in piece 0's slot (piece k's is 2 (D / 4 + 1) 128 float4 further),
-// D / 4 groups of O then (m, l) in the next group, group-major (128 float4
-// apart).  Pieces are combined in piece order, so the result does not depend
-// on which piece finished last: the common maximum and the sum first, then O
-// in groups of 64 columns (16 loads in flight per piece), stored as bf16 to
-// `dst` (nullptr: a padding row, nothing stored).  The merging piece `own`
-// takes its O from TMEM (this row's lane at o_taddr), where it still is,
-// instead of reading back its partial: the same values, 1 / nk fewer bytes.
-// Kept out of line so that its registers do not weigh on the softmax loop's
-// allocation.  Called by whole warps (the TMEM loads are warp-wide).
-template <int D>
-__device__ __noinline__ void merge_pieces_own(const float4* part, int nk, uint4* dst, int own,
-                                          uint32_t o_taddr) {
-  constexpr int NG = D / 4 + 1;
-  const size_t piece_stride = static_cast<size_t>(2) * NG * BM;
-  float m_all = -INFINITY;
-  for (int k = 0; k < nk; ++k) m_all = fmaxf(m_all, __ldcg(part + k * piece_stride + (D / 4) * BM).x);
-  float l_all = 0.f;
-  for (int k = 0; k < nk; ++k) {
-    const float4 ml = __ldcg(part + k * piece_stride + (D / 4) * BM);
-    l_all = fmaf(ml.y, ex2(ml.x - m_all), l_all);
-  }
-  const float inv_l = 1.f / l_all;
-  const uint64_t inv2 = pk2(inv_l, inv_l);
-#pragma unroll
-  for (int cg = 0; cg < D / 64; ++cg) {
-    float acc[64];
-#pragma unroll
-    for (int e = 0; e < 64; ++e) acc[e] = 0.f;
-    for (int k = 0; k < nk; ++k) {
-      const float4* src = part + k * piece_stride;
-      float4 v[16];
-      if (k == own) {
+      if (OWN && k == own) {
         uint32_t t[64];
         tmem_ld32(o_taddr + cg * 64, t);
         tmem_ld32(o_taddr + cg * 64 + 32, t + 32);
@@ -766,6 +708,20 @@ __device__ __noinline__ void merge_pieces_own(const float4* part, int nk, uint4*
       }
     }
   }
+}
+
+// The merge, out of line so that its registers do not weigh on the softmax
+// loop's allocation: every piece read back from the workspace ...
+template <int D>
+__device__ __noinline__ void merge_pieces(const float4* part, int nk, uint4* dst) {
+  merge_rows<D, false>(part, nk, dst, -1, 0u);
+}
+
+// ... or, at D = 64, the merging piece's own O taken from TMEM.
+template <int D>
+__device__ __noinline__ void merge_pieces_own(const float4* part, int nk, uint4* dst, int own,
+                                              uint32_t o_taddr) {
+  merge_rows<D, true>(part, nk, dst, own, o_taddr);
 }
 
 // ----------------------------------------------------------------------------
