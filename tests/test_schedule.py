@@ -95,6 +95,10 @@ def needed_tiles(ids, Np, Nq, q0):
 
 @pytest.mark.parametrize("B,Nq,H,Np,segments,sms", MASKED)
 def test_masked_schedule_covers_every_needed_tile_once(B, Nq, H, Np, segments, sms):
+    check_masked_cover(B, Nq, H, Np, segments, sms)
+
+
+def check_masked_cover(B, Nq, H, Np, segments, sms):
     (rows, grid, slots), ids = masked_sched(B, Nq, H, Np, segments, sms)
     T = -(-Np // 128) + -(-Nq // 128)
     q_pairs = -(-Nq // 256)
@@ -325,6 +329,38 @@ def test_masked_tail_layout(B, Nq, H, Np, segments, sms):
     UNIT_COST positions and then one per visited key tile; CTA c of G holds
     positions [c W / G, (c + 1) W / G) and one item per unit whose tiles meet
     that range, with the visited tiles that fall in it."""
+    check_masked_tail_layout(B, Nq, H, Np, segments, sms)
+
+
+def random_masked_case(seed):
+    """A seeded masked shape: text and image segments over Np + Nq positions
+    (ids -1..3, repeats allowed), a head count that leaves a partial last
+    round, and an SM count from 8 to 160."""
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(1, 4))
+    Nq = int(rng.integers(100, 3000))
+    Np = int(rng.integers(0, 2)) * int(rng.integers(1, 900))
+    sms = int(rng.integers(8, 161))
+    q_pairs = -(-Nq // 256)
+    H = max(1, int(sms * rng.integers(1, 4) + rng.integers(1, sms)) // (B * q_pairs))
+    n, pos, segs = Np + Nq, 0, []
+    while pos < n:
+        L = min(int(rng.integers(1, 700)), n - pos)
+        segs.append((int(rng.integers(-1, 4)) if rng.random() < 0.7 else -1, L))
+        pos += L
+    return B, Nq, H, Np, tuple(segs), sms
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_masked_random_shapes(seed):
+    """Coverage of every needed tile and the exact tail layout on seeded
+    random masked shapes."""
+    case = random_masked_case(4100 + seed)
+    check_masked_cover(*case)
+    check_masked_tail_layout(*case)
+
+
+def check_masked_tail_layout(B, Nq, H, Np, segments, sms):
     (rows, grid, _), ids = masked_sched(B, Nq, H, Np, segments, sms)
     cnt = visited_per_pair(ids, Np, Nq)
     q_pairs, n_bh = len(cnt), B * H
