@@ -403,3 +403,28 @@ def check_masked_tail_layout(B, Nq, H, Np, segments, sms):
         v1 = seen.index(te - 1) + 1
         got[cta].append((b * H + h, q, v0, v1))
     assert dict(got) == dict(expect)
+
+
+def random_dense_case(seed):
+    """A seeded dense shape: units a little past a multiple of the SM count
+    (or below it), any number of key tiles, 4 to 200 SMs."""
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(1, 4))
+    Nq = int(rng.integers(1, 9000))
+    T = int(rng.integers(1, 300))
+    sms = int(rng.integers(4, 201))
+    q_pairs = -(-Nq // 256)
+    target = sms * int(rng.integers(0, 4)) + int(rng.integers(1, sms + 1))
+    H = max(1, target // (B * q_pairs))
+    return B, Nq, H, T, sms
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_dense_random_shapes(seed):
+    """Coverage, item numbering, tail pieces and balance on seeded random
+    dense shapes."""
+    case = random_dense_case(5200 + seed)
+    test_schedule_covers_every_unit_tile_once(*case)
+    test_items_are_numbered_per_cta(*case)
+    test_tail_pieces_partition_their_unit(*case)
+    test_work_is_balanced(*case)
