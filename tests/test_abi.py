@@ -90,6 +90,74 @@ def test_prefix_rejects(lib, args, want):
     assert lib.attn_prefix_fwd(*args, None) == want
 
 
+# Fake image-id and key_valid addresses (16-byte aligned, apart from the tensors).
+IDS, KV = 0x70000000, 0x78000000
+
+
+@pytest.mark.parametrize("args,want", [
+    ((A, B_, C, None, O, 1, 256, 32, 128), ncp.ATTN_ERR_NULL),
+    ((A, None, C, IDS, O, 1, 256, 32, 128), ncp.ATTN_ERR_NULL),
+    ((A, B_, C, IDS + 4, O, 1, 256, 32, 128), ncp.ATTN_ERR_ALIGN),
+    ((A, B_, C, IDS, O, 1, 128 * 1024 + 1, 32, 128), ncp.ATTN_ERR_SHAPE),
+    ((A, B_, C, IDS, O, 1, 0, 32, 128), ncp.ATTN_ERR_SHAPE),
+    ((A, B_, C, IDS, O, 1, 256, 32, 96), ncp.ATTN_ERR_HEADDIM),
+    # out over the id vector, and out over q
+    ((A, B_, C, IDS, IDS - 256 * 32 * 128 * 2 + 16, 1, 256, 32, 128), ncp.ATTN_ERR_ALIAS),
+    ((A, B_, C, IDS, A, 1, 256, 32, 128), ncp.ATTN_ERR_ALIAS),
+])
+def test_block_causal_rejects(lib, args, want):
+    assert lib.attn_block_causal_fwd(*args, None) == want
+
+
+@pytest.mark.parametrize("args,want", [
+    ((A, None, C, O, 1, 128, 512, 32, 64), ncp.ATTN_ERR_NULL),
+    ((A, B_, C, O, 1, 128, 0, 32, 64), ncp.ATTN_ERR_SHAPE),
+    ((A, B_, C, O, 1, 0, 512, 32, 64), ncp.ATTN_ERR_SHAPE),
+    ((A, B_, C, O, 1, 128, 512, 32, 32), ncp.ATTN_ERR_HEADDIM),
+    ((A, B_ + 2, C, O, 1, 128, 512, 32, 64), ncp.ATTN_ERR_ALIGN),
+    ((A, B_, C, B_ + 64, 1, 128, 512, 32, 64), ncp.ATTN_ERR_ALIAS),
+])
+def test_cross_rejects(lib, args, want):
+    assert lib.attn_dense_cross_fwd(*args, None) == want
+
+
+def masked(q=A, kc=B_, vc=C, kp=0x50000000, vp=0x60000000, ids=IDS, kv=KV, scale=0.1, out=O,
+           B=1, Nq=256, Np=128, H=32, D=128):
+    return (q, kc, vc, kp, vp, ids, kv, scale, out, B, Nq, Np, H, D)
+
+
+@pytest.mark.parametrize("args,want", [
+    (masked(ids=None), ncp.ATTN_ERR_NULL),
+    (masked(kc=None), ncp.ATTN_ERR_NULL),
+    (masked(kp=None), ncp.ATTN_ERR_NULL),      # a prefix needs its K and V
+    (masked(ids=IDS + 8), ncp.ATTN_ERR_ALIGN),
+    (masked(scale=0.0), ncp.ATTN_ERR_SHAPE),
+    (masked(scale=-0.1), ncp.ATTN_ERR_SHAPE),
+    (masked(scale=float("inf")), ncp.ATTN_ERR_SHAPE),
+    (masked(scale=float("nan")), ncp.ATTN_ERR_SHAPE),
+    (masked(Np=-1), ncp.ATTN_ERR_SHAPE),
+    (masked(Nq=0), ncp.ATTN_ERR_SHAPE),
+    (masked(Nq=128 * 1024, Np=1), ncp.ATTN_ERR_SHAPE),  # more positions than the tile table
+    (masked(D=48), ncp.ATTN_ERR_HEADDIM),
+    (masked(out=KV - 16), ncp.ATTN_ERR_ALIAS),  # out over key_valid
+    (masked(out=IDS), ncp.ATTN_ERR_ALIAS),      # out over the ids
+    (masked(out=0x50000000), ncp.ATTN_ERR_ALIAS),  # out over the prefix K
+])
+def test_masked_prefix_rejects(lib, args, want):
+    assert lib.attn_masked_prefix_fwd(*args, None) == want
+
+
+@pytest.mark.parametrize("args,want", [
+    ((None, B_, C, O, 1, 128, 32, 64), ncp.ATTN_ERR_NULL),
+    ((A, B_, C, O, 1, 128, 0, 64), ncp.ATTN_ERR_SHAPE),
+    ((A, B_, C, O, 1, 128, 32, 100), ncp.ATTN_ERR_HEADDIM),
+    ((A, B_, C + 4, O, 1, 128, 32, 64), ncp.ATTN_ERR_ALIGN),
+    ((A, B_, C, C, 1, 128, 32, 64), ncp.ATTN_ERR_ALIAS),
+])
+def test_noalloc_rejects(lib, args, want):
+    assert lib.attn_dense_fwd_noalloc(*args, None) == want
+
+
 def test_debug_hook_rejects_unknown_mode(lib):
     assert lib.attn_debug_set_fault(7, 0) == ncp.ATTN_ERR_SHAPE
     assert lib.attn_debug_set_fault(0, 0) == ncp.ATTN_OK
