@@ -141,41 +141,48 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=2)
-        sm, mx, power, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        lines = self.lines
-        in_window = 0
-        if self.window is not None and lines:
-            t0, t1 = self.window
-            # nvidia-smi prints a sample shortly after taking it: allow 0.1 s of lag.
-            inside = [(t, x) for t, x in lines if t0 <= t <= t1 + 0.1]
-            in_window = len(inside)
-            if inside:
-                lines = inside
-            else:
-                # The timed region was shorter than the sampling period: keep
-                # the samples nearest to it (same kernel, taken during the
-                # warm-up just before and the runs just after).
-                mid = 0.5 * (t0 + t1)
-                lines = sorted(lines, key=lambda tx: abs(tx[0] - mid))[:4]
-        for _, line in lines:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-                power.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[4:8]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm), "samples_in_timed_region": in_window,
-                "power_w_max": max(power) if power else None}
+        return summarize_clocks(self.lines, self.window)
+
+
+def summarize_clocks(lines, window):
+    """Median SM clock, max clock, throttle reasons seen and sample counts from
+    timestamped nvidia-smi CSV lines (the ClockSampler.FIELDS columns), taken
+    over the timed region `window` = (t0, t1) host seconds; None without a
+    usable sample."""
+    sm, mx, power, reasons = [], [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    in_window = 0
+    if window is not None and lines:
+        t0, t1 = window
+        # nvidia-smi prints a sample shortly after taking it: allow 0.1 s of lag.
+        inside = [(t, x) for t, x in lines if t0 <= t <= t1 + 0.1]
+        in_window = len(inside)
+        if inside:
+            lines = inside
+        else:
+            # The timed region was shorter than the sampling period: keep
+            # the samples nearest to it (same kernel, taken during the
+            # warm-up just before and the runs just after).
+            mid = 0.5 * (t0 + t1)
+            lines = sorted(lines, key=lambda tx: abs(tx[0] - mid))[:4]
+    for _, line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 8:
+            continue
+        try:
+            sm.append(float(parts[0]))
+            mx.append(float(parts[1]))
+            power.append(float(parts[2]))
+        except ValueError:
+            continue
+        for n, v in zip(names, parts[4:8]):
+            if v.lower().startswith("active"):
+                reasons.add(n)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+            "reasons": sorted(reasons), "samples": len(sm), "samples_in_timed_region": in_window,
+            "power_w_max": max(power) if power else None}
 
 
 def max_over_ranks(value: float, device=None) -> float:
