@@ -56,3 +56,16 @@ def test_single_process_reduction_is_identity():
     import bench
     assert bench.max_over_ranks(3.5) == 3.5
     assert bench.job_throughput(1, 10, 2 * 10 ** 12, 1000.0) == pytest.approx(20.0)
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    """Under torchrun the reference arm (the oracle on the host cores) runs on
+    rank 0 alone: another rank exits 0 at once and prints nothing."""
+    import subprocess
+    import sys
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "1", "--warmup", "3"],
+                         env=env, capture_output=True, text=True, timeout=120)
+    assert res.returncode == 0, res.stderr
+    assert res.stdout.strip() == ""
