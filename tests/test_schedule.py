@@ -428,3 +428,15 @@ def test_dense_random_shapes(seed):
     test_items_are_numbered_per_cta(*case)
     test_tail_pieces_partition_their_unit(*case)
     test_work_is_balanced(*case)
+
+
+def test_block_causal_tail_items_stay_few():
+    """Block-causal N=4448 (text 333, image 2048, text 19, image 2048) on 152
+    SMs: its 120 tail units include many short ones.  With plain visited-tile
+    ranges some CTAs took 7 items and ended last; the unit cost keeps every
+    tail CTA at 3 items or fewer."""
+    (rows, grid, _), _ = masked_sched(1, 4448, 32, 0, ((-1, 333), (0, 2048), (-1, 19), (1, 2048)),
+                                      152)
+    rounds = (32 * 18) // 152
+    items = collections.Counter(int(r[0]) for r in rows if r[1] >= rounds)
+    assert grid == 152 and max(items.values()) <= 3
