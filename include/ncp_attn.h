@@ -23,15 +23,33 @@
  *               fill the last round of SMs, the tail is cut into key-range
  *               pieces on separate SMs whose partial results are merged
  *               through a split workspace: 2 x SMs slots of 2 x 128 x
- *               (128 + 4) floats plus 2 x SMs counters (about 40 MB on a
- *               152-SM GPU), allocated by the first call that splits on each
- *               (device, stream) pair and kept until the process exits.  A
- *               call made while its stream is being captured into a CUDA graph
- *               before that pair has a workspace runs unsplit instead.  A
- *               graph captured after that keeps the capture stream's
- *               workspace: its replays must not run at the same time as other
- *               work using that workspace (calls on the capture stream, or
- *               replays of other graphs captured on it).
+ *               (128 + 4) floats plus 2 x SMs 64-bit counters (about 41 MB
+ *               on a 152-SM GPU).  Workspaces form a pool of at most 4 per
+ *               device, each allocated by the first call that needs it and
+ *               kept until the process exits (at most about 165 MB per
+ *               device, whatever streams come and go).  A call takes the
+ *               workspace its stream used last, else one whose previous
+ *               launch has finished, else a new one while the pool has room;
+ *               when all are busy on other streams it runs without splitting
+ *               (the same result up to rounding order; every call that splits
+ *               gives bit-identical output for the same inputs).  Calls in
+ *               flight at once never share a workspace.  Each launch tags its
+ *               counters with a fresh epoch, so a launch that gave up on a
+ *               bounded wait leaves nothing that affects the next one.
+ *   Graphs:     a call made while its stream is being captured into a CUDA
+ *               graph allocates nothing and queries nothing: it uses the
+ *               workspace that stream used last (make one eager call on the
+ *               capture stream first; otherwise it runs without splitting),
+ *               claims it for good (no other stream takes it afterwards) and
+ *               captures a clear of its counters before the kernel.  The
+ *               graph's replays must not run at the same time as other work
+ *               that uses that workspace: eager calls on the capture stream,
+ *               or replays of other graphs captured on it.
+ *   Reset:      the library keeps per-device state (workspaces, kernel
+ *               attributes, the address of the static scratch of
+ *               attn_dense_fwd_noalloc).  cudaDeviceReset invalidates it: do
+ *               not call the library after resetting a device in the same
+ *               process.
  *   Alignment:  every pointer must be 16-byte aligned (tensor-memory-access
  *               descriptors require it).
  *   Head dim:   D must be 64 or 128; H >= 1 (the definitions fix H = 32, any

@@ -21,7 +21,6 @@
 #include <stdint.h>
 
 #include <cmath>
-#include <map>
 #include <algorithm>
 #include <mutex>
 #include <vector>
@@ -40,7 +39,7 @@
 namespace ncp {
 constexpr int NOALLOC_SLOTS = 320;
 constexpr int NOALLOC_COUNTERS = 320;
-constexpr size_t NOALLOC_COUNT_BYTES = NOALLOC_COUNTERS * sizeof(unsigned int);  // 1280
+constexpr size_t NOALLOC_COUNT_BYTES = NOALLOC_COUNTERS * sizeof(unsigned long long);  // 2560
 constexpr size_t NOALLOC_PART_BYTES =
     static_cast<size_t>(NOALLOC_SLOTS) * 2 * (128 + 4) * BM * sizeof(float);
 constexpr size_t NOALLOC_SCRATCH_BYTES = NOALLOC_COUNT_BYTES + NOALLOC_PART_BYTES;  // 43.3 MB
@@ -187,46 +186,107 @@ size_t part_bytes(long long slots) {
 }
 
 // ---------------------------------------------------------------------------
-// Split workspace: partials of the tail pieces (2 x SMs slots) plus
-// one arrival counter per (tail unit, query tile).  One per (device, stream),
-// so calls that run concurrently on different streams never share one;
-// created on the first call that splits (cudaMalloc, then a zeroing memset on
-// that stream) and kept until the process exits.
+// Split workspaces: partials of the tail pieces (2 x SMs slots) plus one
+// arrival counter per (tail unit, query tile).  A bounded pool per device:
+// at most WS_PER_DEVICE of them, each created by the first call that needs
+// it (cudaMalloc) and kept until the process exits.  A call takes, in this
+// order:
+//   1. the workspace its stream used last;
+//   2. a workspace no other stream has work pending on (its completion
+//      event has fired) and that no graph capture has claimed;
+//   3. a new one, while the pool has room;
+// and otherwise runs without splitting.  The call enqueues a wait on the
+// workspace's completion event (nothing, if it has fired), launches, and
+// records the event again; the pool lock is held throughout, so two calls
+// never take one workspace at once.  Calls that run concurrently on
+// different streams therefore never share a workspace, and the device memory
+// the pool holds is bounded whatever streams come and go.
+//
+// Each launch tags its arrival counters with a fresh epoch (see
+// Params::epoch): a launch that gave up part-way leaves counters that the
+// next one ignores.  A call made while its stream is being captured into a
+// graph uses only a workspace that stream used last, claims it for good (no
+// other stream takes it afterwards) and clears its counters in a captured
+// memset before the kernel, because every replay repeats the captured epoch.
+// Without such a workspace a captured call runs unsplit: nothing is
+// allocated, queried or awaited during a capture.
 // ---------------------------------------------------------------------------
+constexpr int WS_PER_DEVICE = 4;
+
 struct Workspace {
   float* part = nullptr;
-  unsigned int* count = nullptr;
+  unsigned long long* count = nullptr;
+  size_t count_bytes = 0;
+  cudaEvent_t done = nullptr;  // recorded after each launch that used it
+  uintptr_t last_stream = 0;   // stream handle of the last launch that used it
+  bool claimed = false;        // used by a captured graph: only last_stream may take it
+  unsigned int epoch = 0;      // tag of the last launch (0: none yet)
 };
 
 std::mutex g_ws_mutex;
-std::map<std::pair<int, uintptr_t>, Workspace> g_ws;
+std::vector<Workspace*> g_ws[64];  // per device, never shrinks below what it made
 
-const Workspace* get_workspace(int dev, int sms, cudaStream_t stream) {
-  std::lock_guard<std::mutex> lock(g_ws_mutex);
-  const auto key = std::make_pair(dev, reinterpret_cast<uintptr_t>(stream));
-  auto found = g_ws.find(key);
-  if (found != g_ws.end()) return &found->second;
-  // Allocation is not allowed while the stream is being captured into a graph:
-  // then the call runs without splitting.
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
+unsigned int next_epoch(Workspace& ws) {
+  if (++ws.epoch == 0) ws.epoch = 1;  // 0 is a cleared counter's tag
+  return ws.epoch;
+}
+
+// A new workspace on the current device, its counters cleared on `stream`,
+// or nullptr if allocation fails.
+Workspace* new_workspace(int sms, cudaStream_t stream) {
+  Workspace* ws = new Workspace;
+  ws->count_bytes = static_cast<size_t>(2) * sms * sizeof(unsigned long long);
+  if (cudaMalloc(reinterpret_cast<void**>(&ws->part), part_bytes(2LL * sms)) != cudaSuccess ||
+      cudaMalloc(reinterpret_cast<void**>(&ws->count), ws->count_bytes) != cudaSuccess ||
+      cudaMemsetAsync(ws->count, 0, ws->count_bytes, stream) != cudaSuccess ||
+      cudaEventCreateWithFlags(&ws->done, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    if (ws->part) cudaFree(ws->part);
+    if (ws->count) cudaFree(ws->count);
+    delete ws;
+    return nullptr;
+  }
+  return ws;
+}
+
+// Picks this call's workspace from the device's pool (see above) and enqueues
+// what must come before the kernel on `stream`.  Called with g_ws_mutex held;
+// returns nullptr when the call must run unsplit.
+Workspace* take_workspace(int dev, int sms, cudaStream_t stream, bool capturing) {
+  std::vector<Workspace*>& pool = g_ws[dev];
+  const uintptr_t key = reinterpret_cast<uintptr_t>(stream);
+  Workspace* pick = nullptr;
+  for (Workspace* ws : pool)
+    if (ws->last_stream == key) { pick = ws; break; }
+  if (capturing) {
+    if (!pick) return nullptr;
+    if (cudaMemsetAsync(pick->count, 0, pick->count_bytes, stream) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    pick->claimed = true;
+    return pick;
+  }
+  if (!pick) {
+    for (Workspace* ws : pool) {
+      if (ws->claimed) continue;
+      const cudaError_t q = cudaEventQuery(ws->done);
+      if (q == cudaSuccess) { pick = ws; break; }
+      if (q != cudaErrorNotReady) cudaGetLastError();
+    }
+  }
+  if (!pick && static_cast<int>(pool.size()) < WS_PER_DEVICE) {
+    pick = new_workspace(sms, stream);
+    if (pick) pool.push_back(pick);
+  }
+  if (!pick) return nullptr;
+  // Stream-ordered after the workspace's previous launch (a no-op when that
+  // was on this stream, or has finished).
+  if (cudaStreamWaitEvent(stream, pick->done, 0) != cudaSuccess) {
     cudaGetLastError();
     return nullptr;
   }
-  Workspace ws;
-  const size_t count_bytes = static_cast<size_t>(2) * sms * sizeof(unsigned int);
-  if (cudaMalloc(reinterpret_cast<void**>(&ws.part), part_bytes(2LL * sms)) != cudaSuccess) {
-    cudaGetLastError();
-    return nullptr;
-  }
-  if (cudaMalloc(reinterpret_cast<void**>(&ws.count), count_bytes) != cudaSuccess ||
-      cudaMemsetAsync(ws.count, 0, count_bytes, stream) != cudaSuccess) {
-    cudaGetLastError();
-    cudaFree(ws.part);
-    if (ws.count) cudaFree(ws.count);
-    return nullptr;
-  }
-  return &(g_ws[key] = ws);
+  return pick;
 }
 
 // SM count of the current device, with the kernel's shared-memory limit set
@@ -261,15 +321,37 @@ int launch(Params& prm, long long n_units, cudaStream_t stream) {
   if (configure<D, BC>(&dev, &sms) != ATTN_OK) return ATTN_ERR_CUDA;
   const int T = prm.n_tiles[0] + prm.n_tiles[1];
   int grid = make_sched(prm.sc, n_units, T, sms, true, BC);
-  const Workspace* ws = nullptr;
-  if (prm.sc.tail_ctas > 0) {
-    ws = get_workspace(dev, sms, stream);
-    if (!ws) grid = make_sched(prm.sc, n_units, T, sms, false, BC);
+  prm.ws_part = nullptr;
+  prm.ws_count = nullptr;
+  prm.epoch = 1;
+  if (prm.sc.tail_ctas == 0) {
+    ncp::attn_fwd_kernel<D, BC><<<grid, ncp::NUM_THREADS, smem, stream>>>(prm);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
   }
-  prm.ws_part = ws ? ws->part : nullptr;
-  prm.ws_count = ws ? ws->count : nullptr;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  const bool capturing = cap != cudaStreamCaptureStatusNone;
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  Workspace* ws = take_workspace(dev, sms, stream, capturing);
+  if (!ws) {
+    grid = make_sched(prm.sc, n_units, T, sms, false, BC);
+    ncp::attn_fwd_kernel<D, BC><<<grid, ncp::NUM_THREADS, smem, stream>>>(prm);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  }
+  prm.ws_part = ws->part;
+  prm.ws_count = ws->count;
+  prm.epoch = next_epoch(*ws);
   ncp::attn_fwd_kernel<D, BC><<<grid, ncp::NUM_THREADS, smem, stream>>>(prm);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  ws->last_stream = reinterpret_cast<uintptr_t>(stream);
+  if (!capturing && cudaEventRecord(ws->done, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
 }
 
 // Argument checks, TMA descriptors and kernel parameters of one call.
@@ -368,7 +450,8 @@ int launch_noalloc(Params& prm, long long n_units, cudaStream_t stream) {
   if (prm.sc.tail_ctas > 0 &&
       cudaMemsetAsync(scratch, 0, ncp::NOALLOC_COUNT_BYTES, stream) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  prm.ws_count = static_cast<unsigned int*>(scratch);
+  prm.ws_count = static_cast<unsigned long long*>(scratch);
+  prm.epoch = 1;  // the counters were just cleared (tag 0)
   prm.ws_part = reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) +
                                          ncp::NOALLOC_COUNT_BYTES);
   ncp::attn_fwd_kernel<D, false><<<grid, ncp::NUM_THREADS, C::SMEM_BYTES, stream>>>(prm);

@@ -123,7 +123,11 @@ struct Params {
   int Nq, H;
   Sched sc;
   float* ws_part;          // [piece slot][query tile][D / 4 + 1][128 rows][4]: O, then m, l
-  unsigned int* ws_count;  // [tail unit][query tile] finished pieces (reset by the merger)
+  // [tail unit][query tile] arrival counters: (epoch << 32) | pieces counted
+  // in.  A counter whose epoch is not this launch's counts as 0, so a launch
+  // that gave up part-way leaves nothing behind for the next one.
+  unsigned long long* ws_count;
+  unsigned int epoch;      // this launch's tag (never 0: a cleared counter is no launch's)
   int n_tok[2];          // tokens per key segment
   int n_tiles[2];        // KV tiles per key segment
   float scale_log2;      // D^-0.5 * log2(e)
@@ -710,6 +714,24 @@ __device__ __forceinline__ void merge_rows(const float4* part, int nk, uint4* ds
   }
 }
 
+// Counts one piece in on its arrival counter and returns how many pieces of
+// this launch (epoch) were counted in before it, or -1 if the exchange kept
+// failing (it cannot fail more often than there are pieces; the bound only
+// guards the loop).  The counter holds (epoch << 32) | count; a value tagged
+// with another epoch, left by an earlier launch that gave up, counts as 0.
+__device__ __forceinline__ int count_in(unsigned long long* counter, unsigned int epoch) {
+  unsigned long long cur = ld_relaxed_gpu(counter);
+  for (int attempt = 0; attempt < 4 * MAX_PIECES + 64; ++attempt) {
+    const unsigned int cnt =
+        static_cast<unsigned int>(cur >> 32) == epoch ? static_cast<unsigned int>(cur) : 0u;
+    const unsigned long long want = (static_cast<unsigned long long>(epoch) << 32) | (cnt + 1u);
+    const unsigned long long prev = atom_cas_acq_rel_gpu(counter, cur, want);
+    if (prev == cur) return static_cast<int>(cnt);
+    cur = prev;
+  }
+  return -1;
+}
+
 // The merge, out of line so that its registers do not weigh on the softmax
 // loop's allocation: every piece read back from the workspace ...
 template <int D>
@@ -1213,11 +1235,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (ok && lane == 0) {
             // Release this tile's partial (the other warps' writes were
             // acquired through bar_part) and, if last, acquire every piece's.
-            unsigned int* counter = p.ws_count + it.tail * 2 + i;
-            const unsigned int before = atom_add_acq_rel_gpu(counter, 1u);
-            const int last = before == static_cast<unsigned int>(it.pieces - 1);
-            if (last) atomicExch(counter, 0u);  // ready for the next launch
-            ctl->last[i] = last;
+            const int before = count_in(p.ws_count + it.tail * 2 + i, p.epoch);
+            if (before < 0) {
+              *abort_flag = 1;
+              record_timeout(14);
+            }
+            ctl->last[i] = before == it.pieces - 1;
             mbar_arrive(bar_merge);
           }
           __syncwarp();

@@ -100,17 +100,26 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Atomic add with acquire-release semantics at GPU scope: the writes this
-// thread has made or observed before it are visible to whoever acquires the
-// counter after it, and the writes released before the values it reads are
-// visible to this thread after it.
-__device__ __forceinline__ unsigned int atom_add_acq_rel_gpu(unsigned int* addr, unsigned int v) {
-  unsigned int old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
-               : "=r"(old)
-               : "l"(addr), "r"(v)
+// Compare-and-swap of a 64-bit word with acquire-release semantics at GPU
+// scope; returns the old value.  When it succeeds, the writes this thread has
+// made or observed before it are visible to whoever acquires the word after
+// it, and the writes released before the value it read are visible to this
+// thread after it.
+__device__ __forceinline__ unsigned long long atom_cas_acq_rel_gpu(unsigned long long* addr,
+                                                                  unsigned long long cmp,
+                                                                  unsigned long long val) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;"
+               : "=l"(old)
+               : "l"(addr), "l"(cmp), "l"(val)
                : "memory");
   return old;
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu(const unsigned long long* addr) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(addr) : "memory");
+  return v;
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {

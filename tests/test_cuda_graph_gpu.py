@@ -65,3 +65,32 @@ def test_graph_prefix_and_block_causal(cuda_lib):
     eager, replay = capture_and_replay(
         lambda s=None: cuda_lib.attn_block_causal_fwd(q, kc, vc, ids, out2, stream=s), out2)
     assert_parity(f64(replay), f64(eager), "graph replay vs eager (block-causal)")
+
+
+def test_graph_keeps_its_split_workspace(cuda_lib):
+    """Captured on a stream that has just made the same call eagerly, the
+    graph takes that stream's split workspace (and clears its arrival
+    counters in a captured step, since every replay repeats the captured
+    launch): replays are bit-identical to the eager call, also with eager
+    calls on another stream in between, which get a workspace of their own."""
+    w = workloads.custom("dense", 1, 1000, 1000, 4, 128)   # 16 units: split into key pieces
+    q, k, v = (t.cuda() for t in workloads.make_inputs(w, seed_base=17200))
+    out = torch.empty_like(q)
+    other = torch.empty_like(q)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        cuda_lib.attn_dense_fwd(q, k, v, out, stream=s)
+    s.synchronize()
+    eager = out.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        cuda_lib.attn_dense_fwd(q, k, v, out, stream=s)
+    side = torch.cuda.Stream()
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        cuda_lib.attn_dense_fwd(q, k, v, other, stream=side)
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager)
+        assert torch.equal(other, eager)

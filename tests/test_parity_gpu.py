@@ -196,6 +196,33 @@ def test_bounded_wait_reports_timeout(cuda_lib, oracle_mod):
     assert_parity(f64(out), oracle_mod.dense_attention(*bits(ins)), "after timeout")
 
 
+def test_timeout_in_split_launch_leaves_next_call_exact(cuda_lib, oracle_mod):
+    """A launch with a split tail that gives up part-way: block 0 times out in
+    its first unit and never reaches its tail pieces, so the other pieces of
+    those tail units stay counted in.  The next launch on the same workspace
+    tags its counters with a new epoch and must give the same bits as before
+    the fault."""
+    w = workloads.WORKLOADS[2]   # 3 whole rounds, then 56 units split over the SMs
+    ins = workloads.make_inputs(w)
+    q, k, v = to_dev(ins)
+    good = gpu_dense(cuda_lib, q, k, v)
+    assert cuda_lib.device_status()[0] == cuda_lib.ATTN_OK
+    cuda_lib.debug_set_fault(1, 50_000)
+    try:
+        cuda_lib.attn_dense_fwd(q, k, v, torch.empty_like(q))
+        rc, _ = cuda_lib.device_status()
+    finally:
+        cuda_lib.debug_set_fault(0, 0)
+    assert rc == cuda_lib.ATTN_ERR_TIMEOUT
+    for _ in range(2):
+        out = gpu_dense(cuda_lib, q, k, v)
+        assert cuda_lib.device_status()[0] == cuda_lib.ATTN_OK
+        assert torch.equal(out, good)
+    rows = sample_rows(w.B, w.Nq, w.H, n_random=200, seed=22)
+    ref = oracle_mod.dense_attention_rows(*bits(ins), rows)
+    assert_parity(f64(out).reshape(-1, w.D)[rows], ref, "after a split-launch timeout")
+
+
 def test_binding_rejects_bad_tensors(cuda_lib):
     q = torch.zeros(1, 128, 2, 64, device="cuda", dtype=torch.bfloat16)
     with pytest.raises(TypeError):
@@ -243,3 +270,12 @@ def test_workload_sampled(cuda_lib, oracle_mod, cid):
     ref = oracle_mod.dense_attention_rows(*bits(ins), rows)
     s = assert_parity(got, ref, w.describe())
     print(w.name, s)
+    if cid == 5:
+        # Negative controls on the same rows: an all-zero output and the mean
+        # of V (a kernel blind to Q K^T) must fail the gate, although the
+        # mean of V passes the element rule here (|O| ~ 3e-3 < atol).
+        with pytest.raises(AssertionError):
+            assert_parity(np.zeros_like(got), ref, "all-zero control")
+        mean_v = f64(ins[2][0].cuda().float().mean(0))  # [H, D]
+        with pytest.raises(AssertionError):
+            assert_parity(mean_v[rows % w.H], ref, "mean-of-V control")
