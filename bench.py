@@ -4,7 +4,8 @@
 One step = one call of the hot path (attn_dense_fwd, or attn_prefix_fwd for
 the prefix workload) over one batch of seeded synthetic bf16 inputs.  The
 metric is TFLOP/s with FLOPs = 4 * B * H * Nq * Nkv * D (2*D per score for
-Q K^T, 2*D for P V).  The default workload is dense B=1 N=4096 H=32 D=128.
+Q K^T, 2*D for P V).  The default workload is the largest single-GPU one,
+dense B=1 N=32768 H=32 D=128 (inputs N(0, 0.5^2)).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload ID]
     python bench.py --impl reference ...   # the FP64 CPU oracle, same metric
@@ -75,19 +76,49 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload_name: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source (else None)."""
+def recorded_profile(workload_name: str) -> dict:
+    """The committed ncu figures of one launch of the workload's kernel
+    (profiles/traffic.json), if they were taken on the current kernel source;
+    else {}.  Keys: dram_bytes_per_launch, and where captured
+    tensor_pipe_active_pct and duration_us."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             doc = json.load(f)
     except (OSError, ValueError):
-        return None
+        return {}
     ent = doc.get(workload_name)
     if not ent or ent.get("kernel_source_hash") != kernel_source_hash():
-        return None
-    return ent.get("dram_bytes_per_launch")
+        return {}
+    return ent
+
+
+def recorded_traffic(workload_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    return recorded_profile(workload_name).get("dram_bytes_per_launch")
+
+
+NOMINAL_HBM_GBS = 8000.0
+
+
+def ncu_fields(workload_name: str, hbm_peak_gbs: float) -> dict:
+    """The ncu figures the line carries beside the roofline: tensor-pipe
+    utilisation and DRAM GB/s (against the nominal 8 TB/s and the measured
+    copy bandwidth), from one ncu capture of the current source; None where
+    no such capture is recorded."""
+    ent = recorded_profile(workload_name)
+    dram = ent.get("dram_bytes_per_launch")
+    dur = ent.get("duration_us")
+    gbs = dram / (dur * 1e-6) / 1e9 if dram and dur else None
+    return {
+        "tensor_pipe_active_pct": ent.get("tensor_pipe_active_pct"),
+        "dram_gbs": round(gbs, 1) if gbs else None,
+        "dram_frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4) if gbs else None,
+        "dram_frac_of_measured": round(gbs / hbm_peak_gbs, 4) if gbs else None,
+        "ncu_source": "profiles/traffic.json (one ncu launch, --clock-control none)"
+                      if ent else None,
+    }
 
 
 class ClockSampler:
@@ -393,7 +424,14 @@ def run_gpu(args):
 
     peaks, peak_src = measured_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_BF16_TFLOPS))
-    achieved = w.flops / (statistics.mean(times) / 1e3) / 1e12
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    # `value` and `roofline.achieved` both use the mean launch time (total
+    # over the K timed launches); the median, the statistic of the pages'
+    # audit timing, is reported beside them.
+    mean_ms = statistics.mean(times)
+    median_ms = statistics.median(times)
+    achieved = w.flops / (mean_ms / 1e3) / 1e12
+    achieved_median = w.flops / (median_ms / 1e3) / 1e12
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -414,15 +452,28 @@ def run_gpu(args):
             "l2": "512 MiB buffer written before every timed launch (inputs < L2)",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
+        "timing": {
+            "statistic": "value and roofline.achieved: mean of the K per-launch CUDA-event "
+                         "times; *_median: their median",
+            "mean_ms": round(mean_ms, 5),
+            "median_ms": round(median_ms, 5),
+            "min_ms": round(min(times), 5),
+            "max_ms": round(max(times), 5),
+            "value_median": round(achieved_median * world, 2),
+        },
         "roofline": {
             "bound": "tensor",
             "achieved": round(achieved, 2),
+            "achieved_median": round(achieved_median, 2),
             "peak": peak,
             "unit": UNIT,
             "frac": round(achieved / peak, 4),
+            "frac_median": round(achieved_median / peak, 4),
             "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)",
             "kernel": KERNEL_NAME + ("<128>" if w.D == 128 else "<64>"),
             "traffic": recorded_traffic(w.name),
+            "algorithmic_bytes": w.hbm_bytes,
+            **ncu_fields(w.name, hbm_peak),
         },
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
@@ -452,8 +503,10 @@ def per_config(torch, ncp, flush, stream, peak, args):
         times, _ = time_device(torch, call, flush, steps, 3, stream)
         us = statistics.median(times) * 1e3
         tf = w.flops / (us / 1e6) / 1e12
-        res[w.name] = {"median_us": round(us, 2), "tflops": round(tf, 1),
-                       "frac_of_peak": round(tf / peak, 4)}
+        res[w.name] = {"median_us": round(us, 2), "mean_us": round(statistics.mean(times) * 1e3, 2),
+                       "tflops": round(tf, 1), "frac_of_peak": round(tf / peak, 4),
+                       "tensor_pipe_active_pct": recorded_profile(w.name).get(
+                           "tensor_pipe_active_pct")}
         del dev_in, out
     torch.cuda.empty_cache()
     return res
@@ -513,7 +566,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", type=int, default=2, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", type=int, default=5, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config table")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
