@@ -11,6 +11,7 @@ namespace ncp {
 constexpr int BM = 128;                  // query rows per tile (one TMEM lane each)
 constexpr int BN = 128;                  // keys per KV tile
 constexpr int NUM_THREADS = 320;
+constexpr int PAIR_THREADS = 320;        // the CTA-pair kernel
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr uint32_t TMEM_COLS = 512;
@@ -100,8 +101,9 @@ struct SharedCtl {
 // tiles), n_units = B * H * q_pairs of them; see schedule_item.
 struct Sched {
   int n_units;
-  int q_pairs;     // ceil(Nq / 256): units per (b, h); q pair fastest
+  int q_pairs;     // ceil(Nq / unit_rows): units per (b, h); query block fastest
   int H, Nq;
+  int unit_rows;   // query rows per unit: 256 (one CTA, two 128-row tiles) or 512 (a CTA pair)
   int n_whole;     // units walked whole
   int tail_units;  // units after them, cut into key ranges (0: none)
   int tail_ctas;   // CTAs sharing the tail (0: no tail)
@@ -114,6 +116,7 @@ struct Params {
   CUtensorMap tm_q;
   CUtensorMap tm_k[2];   // [0] prefix segment, [1] current segment
   CUtensorMap tm_v[2];
+  CUtensorMap tm_kh[2];  // CTA-pair kernel: K with 64-token boxes (half a key tile per CTA)
   __nv_bfloat16* out;
   // Masked forms (block-causal, masked prefix-cached): image id per key
   // position [Np + Nq] (-1 = text) and, optionally, key_valid [B, Np + Nq]
@@ -199,8 +202,8 @@ __host__ __device__ __forceinline__ Unit decode_unit(const Sched& s, bool bc, in
   }
   u.h = bh % s.H;
   u.b = bh / s.H;
-  u.q0 = qp * (2 * BM);
-  u.two = (u.q0 + BM) < s.Nq;
+  u.q0 = qp * s.unit_rows;
+  u.two = (u.q0 + s.unit_rows / 2) < s.Nq;
   return u;
 }
 
@@ -654,11 +657,12 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, i
 // `own` takes its O from TMEM (this row's lane at o_taddr), where it still
 // is, instead of reading back its partial: the same values, 1 / nk fewer
 // bytes (called by whole warps then: the TMEM loads are warp-wide).
-template <int D, bool OWN>
+template <int D, bool OWN, int SLOT_CTAS = 1>
 __device__ __forceinline__ void merge_rows(const float4* part, int nk, uint4* dst, int own,
                                            uint32_t o_taddr) {
   constexpr int NG = D / 4 + 1;
-  const size_t piece_stride = static_cast<size_t>(2) * NG * BM;
+  // A slot holds SLOT_CTAS CTAs' partials (1; 2 for a CTA pair) of 2 tiles each.
+  const size_t piece_stride = static_cast<size_t>(2) * SLOT_CTAS * NG * BM;
   float m_all = -INFINITY;
   for (int k = 0; k < nk; ++k) m_all = fmaxf(m_all, __ldcg(part + k * piece_stride + (D / 4) * BM).x);
   float l_all = 0.f;
@@ -734,9 +738,9 @@ __device__ __forceinline__ int count_in(unsigned long long* counter, unsigned in
 
 // The merge, out of line so that its registers do not weigh on the softmax
 // loop's allocation: every piece read back from the workspace ...
-template <int D>
+template <int D, int SLOT_CTAS = 1>
 __device__ __noinline__ void merge_pieces(const float4* part, int nk, uint4* dst) {
-  merge_rows<D, false>(part, nk, dst, -1, 0u);
+  merge_rows<D, false, SLOT_CTAS>(part, nk, dst, -1, 0u);
 }
 
 // ... or, at D = 64, the merging piece's own O taken from TMEM.
@@ -902,9 +906,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // MMA issuer waits until the softmax warps have worked the tail items out.
   const int tail_rounds = p.sc.tail_ctas ? p.sc.n_whole / static_cast<int>(gridDim.x) : 0;
   const uint32_t bar_tail = smem_u32(&ctl->tail_ready);
+  // (Called by the loader and the MMA issuer, whole warps.)
   auto await_tail = [&](int n, int site) -> bool {
     if (!masked_tail || n < tail_rounds || mtail.n_items > 0) return true;
-    if (!wait_bounded(bar_tail, 0, limit, abort_flag, site)) return false;
+    if (!warp_wait(bar_tail, 0, limit, abort_flag, site)) return false;
     mtail.n_items = ctl->n_tail_items;
     return true;
   };
@@ -914,12 +919,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == PRODUCER_WARP) {
     // ---------------------------------------------------------------- loader
+    // The whole warp runs the loop, converged; one elected lane issues each
+    // copy (see mma_ss_elect).
     if (lane == 0) {
       prefetch_tmap(&p.tm_q);
       for (int s = 0; s < 2; ++s) {
         prefetch_tmap(&p.tm_k[s]);
         prefetch_tmap(&p.tm_v[s]);
       }
+    }
+    __syncwarp();
+    {
       int slot = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -928,15 +938,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const Unit& u = it.u;
         // The Q buffers are free once every S MMA of the previous item is done.
         if (n > 0) {
-          ok = wait_bounded(bar_qfree, (n - 1) & 1, limit, abort_flag, 9);
+          ok = warp_wait(bar_qfree, (n - 1) & 1, limit, abort_flag, 9);
           if (!ok) break;
         }
         const int nq_tiles = u.two ? 2 : 1;
-        mbar_expect_tx(bar_q, nq_tiles * C::TILE_BYTES);
+        mbar_expect_tx_elect(bar_q, nq_tiles * C::TILE_BYTES);
         for (int i = 0; i < nq_tiles; ++i)
           for (int c = 0; c < C::CHUNKS; ++c)
-            tma_load_4d(qs + i * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tm_q, c * 64, u.h,
-                        u.q0 + i * BM, u.b, bar_q);
+            tma_load_4d_elect(qs + i * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tm_q, c * 64, u.h,
+                              u.q0 + i * BM, u.b, bar_q);
         q_last = n;
 #pragma unroll 1
         for (int t = it.t_begin; t < it.t_end && ok; ++t) {
@@ -944,15 +954,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int seg = (t < T0) ? 0 : 1;
           const int tok0 = (t - (seg ? T0 : 0)) * BN;
           for (int kind = 0; kind < 2; ++kind) {
-            ok = wait_bounded(bar_kv_empty(slot), phase ^ 1u, limit, abort_flag, 1);
+            ok = warp_wait(bar_kv_empty(slot), phase ^ 1u, limit, abort_flag, 1);
             if (!ok) break;
             const bool skip = (p.fault_mode == 1) && kind == 1 && t == 1 && n == 0 && blockIdx.x == 0;
             if (!skip) {
               const CUtensorMap* map = kind == 0 ? &p.tm_k[seg] : &p.tm_v[seg];
-              mbar_expect_tx(bar_kv_full(slot), C::TILE_BYTES);
+              mbar_expect_tx_elect(bar_kv_full(slot), C::TILE_BYTES);
               for (int c = 0; c < C::CHUNKS; ++c)
-                tma_load_4d(ring + slot * C::TILE_BYTES + c * C::CHUNK_BYTES, map, c * 64, u.h,
-                            tok0, u.b, bar_kv_full(slot));
+                tma_load_4d_elect(ring + slot * C::TILE_BYTES + c * C::CHUNK_BYTES, map, c * 64,
+                                  u.h, tok0, u.b, bar_kv_full(slot));
               ld_issued |= 1u << slot;
               ld_parity = (ld_parity & ~(1u << slot)) | (phase << slot);
             }
@@ -967,7 +977,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop, converged (warp-wide bounded waits); one
+    // elected lane issues each MMA and commit (see mma_ss_elect).
+    {
       constexpr uint32_t IDESC_S = make_idesc(BM, BN, false);
       constexpr uint32_t IDESC_PV = make_idesc(BM, D, true);
       // S_i = Q_i K^T over D in K-steps of 16 (32 bytes inside a 128-byte row).
@@ -977,8 +989,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-          mma_ss(tmem + tmem_s_col(i), sw128_desc(qa + off, 16, 1024),
-                 sw128_desc(kb + off, 16, 1024), IDESC_S, kk > 0);
+          mma_ss_elect(tmem + tmem_s_col(i), sw128_desc(qa + off, 16, 1024),
+                       sw128_desc(kb + off, 16, 1024), IDESC_S, kk > 0);
         }
       };
       // O_i += P_i V over the BN keys in K-steps of 16 rows of V (MN-major B).
@@ -986,9 +998,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t vb = ring + v_slot * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tmem + tmem_o_col(i), tmem + tmem_s_col(i) + kk * 8,
-                 sw128_desc(vb + kk * 16 * 128, C::CHUNK_BYTES, 1024), IDESC_PV,
-                 (accumulate || kk > 0) ? 1u : 0u);
+          mma_ts_elect(tmem + tmem_o_col(i), tmem + tmem_s_col(i) + kk * 8,
+                       sw128_desc(vb + kk * 16 * 128, C::CHUNK_BYTES, 1024), IDESC_PV,
+                       (accumulate || kk > 0) ? 1u : 0u);
       };
 
       int slot = 0;
@@ -999,9 +1011,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // The first P V of a unit overwrites O_i: wait until the epilogue of the
       // previous unit has read it out of TMEM.
       auto pv = [&](int i, int v_slot, bool accumulate) -> bool {
-        if (!wait_bounded(bar_p(i), (sc[i] - 1u) & 1u, limit, abort_flag, 4)) return false;
+        if (!warp_wait(bar_p(i), (sc[i] - 1u) & 1u, limit, abort_flag, 4)) return false;
         if (!accumulate && oc[i] > 0 &&
-            !wait_bounded(bar_ofree(i), (oc[i] - 1u) & 1u, limit, abort_flag, 6))
+            !warp_wait(bar_ofree(i), (oc[i] - 1u) & 1u, limit, abort_flag, 6))
           return false;
         tc_fence_after();
         issue_pv(i, v_slot, accumulate);
@@ -1010,7 +1022,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       Item it;
       for (int n = 0; ok && (ok = await_tail(n, 13)) && get_item<BC>(p, &mtail, T, n, it); ++n) {
         const int nq = it.u.two ? 2 : 1;
-        ok = wait_bounded(bar_q, n & 1, limit, abort_flag, 2);
+        ok = warp_wait(bar_q, n & 1, limit, abort_flag, 2);
         if (!ok) break;
         int v_prev = -1;
         int j = 0;  // key tiles visited so far in this item
@@ -1018,7 +1030,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int t = it.t_begin; t < it.t_end && ok; ++t) {
           if (BC && !bc_unit_visits(tt, p, it.u, t)) continue;
           const int k_slot = slot;
-          ok = wait_bounded(bar_kv_full(k_slot), phase, limit, abort_flag, 3);
+          ok = warp_wait(bar_kv_full(k_slot), phase, limit, abort_flag, 3);
           if (!ok) break;
           if (++slot == C::NSLOT) { slot = 0; phase ^= 1u; }
           tc_fence_after();
@@ -1032,30 +1044,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (!ok) break;
             }
             issue_s(i, k_slot);
-            mma_commit(bar_s(i));
+            mma_commit_elect(bar_s(i));
             ++sc[i];
           }
           if (!ok) break;
-          if (j > 0) mma_commit(bar_kv_empty(v_prev));
-          mma_commit(bar_kv_empty(k_slot));
+          if (j > 0) mma_commit_elect(bar_kv_empty(v_prev));
+          mma_commit_elect(bar_kv_empty(k_slot));
           const int v_slot = slot;
-          ok = wait_bounded(bar_kv_full(v_slot), phase, limit, abort_flag, 5);
+          ok = warp_wait(bar_kv_full(v_slot), phase, limit, abort_flag, 5);
           if (!ok) break;
           if (++slot == C::NSLOT) { slot = 0; phase ^= 1u; }
           v_prev = v_slot;
           ++j;
         }
         if (!ok) break;
-        mma_commit(bar_qfree);  // every S MMA of this item has been issued
+        mma_commit_elect(bar_qfree);  // every S MMA of this item has been issued
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           if (i >= nq || !ok) break;
           ok = pv(i, v_prev, j - 1 > 0);
           if (!ok) break;
-          mma_commit(bar_o(i));
+          mma_commit_elect(bar_o(i));
           ++oc[i];
         }
-        if (ok) mma_commit(bar_kv_empty(v_prev));
+        if (ok) mma_commit_elect(bar_kv_empty(v_prev));
       }
     }
     __syncwarp();
@@ -1291,9 +1303,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int s = 0; s < C::NSLOT; ++s)
         if (ld_issued & (1u << s)) wait_drain(bar_kv_full(s), (ld_parity >> s) & 1u, limit);
     }
-    if (warp == MMA_WARP && lane == 0) {
-      mma_commit(smem_u32(&ctl->drain));
-      wait_drain(smem_u32(&ctl->drain), 0, limit);
+    if (warp == MMA_WARP) {
+      // The MMAs were issued by the elected lane: commit from it too.
+      mma_commit_elect(smem_u32(&ctl->drain));
+      if (lane == 0) wait_drain(smem_u32(&ctl->drain), 0, limit);
     }
     __syncwarp();
   }
