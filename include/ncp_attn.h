@@ -212,16 +212,6 @@ int attn_device_status(cudaStream_t stream, unsigned int *info);
 int attn_debug_set_fault(int mode, unsigned int wait_limit_us);
 
 /*
- * Test hook: which kernel runs the calls whose keys are all visible (dense,
- * cross, prefix-cached and attn_dense_fwd_noalloc).  mode 0: automatic (D =
- * 128 runs on CTA pairs, D = 64 on single CTAs); 1: single CTAs only; 2: CTA
- * pairs wherever they apply (D = 128).  Host-side setting for subsequent
- * calls of this process.  Returns ATTN_OK, or ATTN_ERR_SHAPE for an unknown
- * mode.
- */
-int attn_debug_set_path(int mode);
-
-/*
  * Test hook: y[i] = 2^x[i] for i < n through one of the two exponential paths
  * of the softmax: mode 0 the FMA-pipe polynomial (Cody-Waite reduction and a
  * minimax cubic, relative error <= 1.02e-4 for -126 <= x <= 127, exactly 0 for
@@ -234,9 +224,7 @@ int attn_debug_exp2(const float *x, float *y, long long n, int mode, cudaStream_
 /*
  * Test hook: the work schedule of a launch, computed on the host without a
  * GPU.  masked = 0: the dense family (dense, cross, prefix-cached) with
- * n_key_tiles key tiles of 128 (image_ids and Np ignored); masked = 2: the
- * same on CTA pairs (units of 512 query rows; `sms` is then the number of
- * pairs and a row's cta is a pair).  masked = 1: the
+ * n_key_tiles key tiles of 128 (image_ids and Np ignored).  masked = 1: the
  * block-causal and masked prefix forms, Np prefix positions then Nq current
  * ones, image_ids a host array of Np + Nq ids (caller-owned; the key tiles
  * are counted from Np and Nq, n_key_tiles is ignored).  A launch over B

@@ -13,7 +13,7 @@ from ._binding import (  # noqa: F401
     ATTN_ERR_SHAPE, ATTN_ERR_TIMEOUT, ATTN_OK, SIGNATURES, AttnError, attn_dense_fwd,
     attn_block_causal_fwd, attn_dense_cross_fwd, attn_dense_fwd_noalloc, attn_masked_prefix_fwd,
     block_causal_attention,
-    attn_prefix_fwd, debug_exp2, debug_schedule, debug_set_fault, debug_set_path, dense_attention, device_status,
+    attn_prefix_fwd, debug_exp2, debug_schedule, debug_set_fault, dense_attention, device_status,
     library_path,
     load_library, prefix_attention, status_string,
 )

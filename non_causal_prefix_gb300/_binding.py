@@ -29,7 +29,6 @@ SIGNATURES = {
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_device_status": (_I, [_VP, _UIP]),
     "attn_debug_set_fault": (_I, [_I, ctypes.c_uint]),
-    "attn_debug_set_path": (_I, [_I]),
     "attn_debug_exp2": (_I, [_VP, _VP, ctypes.c_longlong, _I, _VP]),
     "attn_debug_schedule": (_I, [_I, _I, _I, _I, _I, _I, _VP, _I, _VP, _I, _VP, _VP, _VP]),
     "attn_dense_fwd_noalloc": (_I, [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP]),
@@ -270,19 +269,13 @@ def debug_set_fault(mode: int, wait_limit_us: int = 0) -> None:
            "attn_debug_set_fault")
 
 
-def debug_set_path(mode: int) -> None:
-    """0: automatic kernel choice; 1: single-CTA kernel only; 2: CTA pairs where they apply."""
-    _check(load_library().attn_debug_set_path(int(mode)), "attn_debug_set_path")
-
-
 def debug_schedule(B: int, Nq: int, H: int, n_key_tiles: int, sms: int, masked: bool = False,
-                   image_ids=None, Np: int = 0, pairs: bool = False):
+                   image_ids=None, Np: int = 0):
     """The launch schedule for these sizes on a GPU with `sms` SMs, computed on
     the host: (rows, grid, slots) with rows an int32 array [items, 12] of
     (cta, n, b, h, q0, two, t_begin, t_end, tail, piece, pieces, slot0).
     Masked forms take image_ids (Np + Nq ints) and Np; n_key_tiles is then
-    ignored.  pairs: the dense family on CTA pairs, `sms` pairs of units of
-    512 query rows (cta is then a pair)."""
+    ignored."""
     import numpy as np
     lib = load_library()
     ids = None
@@ -292,8 +285,8 @@ def debug_schedule(B: int, Nq: int, H: int, n_key_tiles: int, sms: int, masked: 
             raise ValueError("image_ids must hold Np + Nq ids")
     ids_ptr = ids.ctypes.data if ids is not None else None
     n_rows, grid, slots = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
-    mode = 1 if masked else (2 if pairs else 0)
-    args = (int(B), int(Nq), int(H), int(n_key_tiles), int(sms), mode, ids_ptr, int(Np))
+    args = (int(B), int(Nq), int(H), int(n_key_tiles), int(sms), 1 if masked else 0, ids_ptr,
+            int(Np))
     rc = lib.attn_debug_schedule(*args, None, 0, ctypes.byref(n_rows), ctypes.byref(grid),
                                  ctypes.byref(slots))
     if rc not in (0, -2) or (rc == -2 and n_rows.value == 0):

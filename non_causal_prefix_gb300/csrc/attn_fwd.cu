@@ -28,7 +28,6 @@
 
 #include "ncp_attn.h"
 #include "attn_kernel.cuh"
-#include "attn_pair_kernel.cuh"
 
 // ============================================================================
 // Fixed scratch for attn_dense_fwd_noalloc: the split workspace (arrival
@@ -76,12 +75,10 @@ EncodeTiledFn encode_fn() {
 std::mutex g_cfg_mutex;
 int g_fault_mode = 0;
 unsigned long long g_wait_limit_ns = 2000000000ull;
-int g_path_mode = 0;  // 0: automatic, 1: one-CTA kernel only, 2: CTA-pair kernel where it applies
 
-// [B, N, H, D] bf16, box of 64 head-dim elements x 1 head x box_rows tokens x
-// 1 batch, 128-byte swizzle, zero fill out of bounds.
-bool make_map(CUtensorMap* map, const void* base, int B, int N, int H, int D,
-              unsigned box_rows = 128) {
+// [B, N, H, D] bf16, box of 64 head-dim elements x 1 head x 128 tokens x 1
+// batch, 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap* map, const void* base, int B, int N, int H, int D) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
@@ -89,7 +86,7 @@ bool make_map(CUtensorMap* map, const void* base, int B, int N, int H, int D,
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
                                  static_cast<cuuint64_t>(H) * D * 2,
                                  static_cast<cuuint64_t>(N) * H * D * 2};
-  const cuuint32_t box[4] = {64, 1, box_rows, 1};
+  const cuuint32_t box[4] = {64, 1, 128, 1};
   const cuuint32_t estride[4] = {1, 1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
              estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -357,107 +354,6 @@ int launch(Params& prm, long long n_units, cudaStream_t stream) {
   return ATTN_OK;
 }
 
-// The CTA-pair kernel on the current device: its shared-memory limit set and
-// the number of pairs that can be resident at once (one CTA per SM), found
-// once per device.
-int configure_pair(int* dev_out, int* pairs_out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
-  static int pair_count[64] = {};
-  if (dev < 0 || dev >= 64) return ATTN_ERR_CUDA;
-  if (pair_count[dev] == 0) {
-    if (cudaFuncSetAttribute(ncp::attn_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             ncp::PairCfg::SMEM_BYTES) != cudaSuccess)
-      return ATTN_ERR_CUDA;
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 2)
-      return ATTN_ERR_CUDA;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
-    cfg.blockDim = dim3(ncp::PAIR_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = ncp::PairCfg::SMEM_BYTES;
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, ncp::attn_pair_kernel, &cfg) != cudaSuccess ||
-        clusters < 1) {
-      cudaGetLastError();
-      clusters = sms / 2;
-    }
-    pair_count[dev] = clusters < sms / 2 ? clusters : sms / 2;
-  }
-  *dev_out = dev;
-  *pairs_out = pair_count[dev];
-  return ATTN_OK;
-}
-
-// Units of 512 query rows on CTA pairs: the schedule of launch<D, BC> with
-// pairs in place of CTAs (a pair's piece of a tail unit takes two workspace
-// slots, one per CTA, and four counters per tail unit).
-int launch_pair(Params& prm, cudaStream_t stream) {
-  int dev = 0, pairs = 0;
-  if (configure_pair(&dev, &pairs) != ATTN_OK) return ATTN_ERR_CUDA;
-  int sms = 0;
-  if (configure<128, false>(&dev, &sms) != ATTN_OK) return ATTN_ERR_CUDA;
-  const int T = prm.n_tiles[0] + prm.n_tiles[1];
-  const long long q_blocks = (static_cast<long long>(prm.Nq) + 4 * ncp::BM - 1) / (4 * ncp::BM);
-  const long long n_units = static_cast<long long>(prm.sc.n_units / prm.sc.q_pairs) * q_blocks;
-  prm.sc.q_pairs = static_cast<int>(q_blocks);
-  prm.sc.unit_rows = 4 * ncp::BM;
-  int grid = make_sched(prm.sc, n_units, T, pairs, true, false);
-  prm.ws_part = nullptr;
-  prm.ws_count = nullptr;
-  prm.epoch = 1;
-  constexpr uint32_t smem = ncp::PairCfg::SMEM_BYTES;
-  if (prm.sc.tail_ctas == 0) {
-    ncp::attn_pair_kernel<<<2 * grid, ncp::PAIR_THREADS, smem, stream>>>(prm);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
-  }
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
-    cudaGetLastError();
-    return ATTN_ERR_CUDA;
-  }
-  const bool capturing = cap != cudaStreamCaptureStatusNone;
-  std::lock_guard<std::mutex> lock(g_ws_mutex);
-  Workspace* ws = take_workspace(dev, sms, stream, capturing);
-  if (!ws) {
-    grid = make_sched(prm.sc, n_units, T, pairs, false, false);
-    ncp::attn_pair_kernel<<<2 * grid, ncp::PAIR_THREADS, smem, stream>>>(prm);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
-  }
-  prm.ws_part = ws->part;
-  prm.ws_count = ws->count;
-  prm.epoch = next_epoch(*ws);
-  ncp::attn_pair_kernel<<<2 * grid, ncp::PAIR_THREADS, smem, stream>>>(prm);
-  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-  ws->last_stream = reinterpret_cast<uintptr_t>(stream);
-  if (!capturing && cudaEventRecord(ws->done, stream) != cudaSuccess) {
-    cudaGetLastError();
-    return ATTN_ERR_CUDA;
-  }
-  return ATTN_OK;
-}
-
-// Whether a call runs on the CTA-pair kernel: only when a test forces it
-// (attn_debug_set_path(2)), for D = 128 with every key visible (the dense,
-// cross and prefix-cached forms).  Builds the pair kernel's K maps when it does.
-bool use_pair(Params& prm, const void* kp, const void* kc, int B, int Np, int Nc, int H, int D,
-              bool masked) {
-  if (masked || D != 128) return false;
-  int mode = 0;
-  {
-    std::lock_guard<std::mutex> lock(g_cfg_mutex);
-    mode = g_path_mode;
-  }
-  if (mode != 2) return false;
-  if (!make_map(&prm.tm_kh[1], kc, B, Nc, H, D, 64)) return false;
-  if (Np > 0) {
-    if (!make_map(&prm.tm_kh[0], kp, B, Np, H, D, 64)) return false;
-  } else {
-    prm.tm_kh[0] = prm.tm_kh[1];
-  }
-  return true;
-}
-
 // Argument checks, TMA descriptors and kernel parameters of one call.
 int prepare(const void* q, const void* kp, const void* vp, const void* kc, const void* vc,
             const int* image_ids, const unsigned char* key_valid, float sm_scale, void* out, int B,
@@ -563,33 +459,6 @@ int launch_noalloc(Params& prm, long long n_units, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-// launch_pair with the split workspace in the static scratch (two CTA slots
-// per pair slot, four counters per tail unit).
-int launch_pair_noalloc(Params& prm, cudaStream_t stream) {
-  int dev = 0, pairs = 0, sms = 0;
-  if (configure_pair(&dev, &pairs) != ATTN_OK) return ATTN_ERR_CUDA;
-  if (configure<128, false>(&dev, &sms) != ATTN_OK) return ATTN_ERR_CUDA;
-  const int T = prm.n_tiles[0] + prm.n_tiles[1];
-  const long long q_blocks = (static_cast<long long>(prm.Nq) + 4 * ncp::BM - 1) / (4 * ncp::BM);
-  const long long n_units = static_cast<long long>(prm.sc.n_units / prm.sc.q_pairs) * q_blocks;
-  prm.sc.q_pairs = static_cast<int>(q_blocks);
-  prm.sc.unit_rows = 4 * ncp::BM;
-  const int grid = make_sched(prm.sc, n_units, T, pairs, true, false);
-  if (2 * sched_slots(prm.sc) > ncp::NOALLOC_SLOTS || 4 * prm.sc.tail_units > ncp::NOALLOC_COUNTERS)
-    return ATTN_ERR_SHAPE;
-  void* scratch = nullptr;
-  if (noalloc_scratch(dev, &scratch) != ATTN_OK) return ATTN_ERR_CUDA;
-  if (prm.sc.tail_ctas > 0 &&
-      cudaMemsetAsync(scratch, 0, ncp::NOALLOC_COUNT_BYTES, stream) != cudaSuccess)
-    return ATTN_ERR_CUDA;
-  prm.ws_count = static_cast<unsigned long long*>(scratch);
-  prm.epoch = 1;
-  prm.ws_part = reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) +
-                                         ncp::NOALLOC_COUNT_BYTES);
-  ncp::attn_pair_kernel<<<2 * grid, ncp::PAIR_THREADS, ncp::PairCfg::SMEM_BYTES, stream>>>(prm);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
-}
-
 int run(const void* q, const void* kp, const void* vp, const void* kc, const void* vc,
         const int* image_ids, const unsigned char* key_valid, float sm_scale, void* out, int B,
         int Nq, int Np, int Nc, int H, int D, cudaStream_t stream) {
@@ -601,7 +470,6 @@ int run(const void* q, const void* kp, const void* vp, const void* kc, const voi
   if (image_ids)
     return D == 128 ? launch<128, true>(prm, n_units, stream)
                     : launch<64, true>(prm, n_units, stream);
-  if (use_pair(prm, kp, kc, B, Np, Nc, H, D, false)) return launch_pair(prm, stream);
   return D == 128 ? launch<128, false>(prm, n_units, stream)
                   : launch<64, false>(prm, n_units, stream);
 }
@@ -662,7 +530,6 @@ int attn_dense_fwd_noalloc(const void* q, const void* k, const void* v, void* ou
   const int rc =
       prepare(q, nullptr, nullptr, k, v, nullptr, nullptr, 0.f, out, B, N, 0, N, H, D, prm, n_units);
   if (rc != ATTN_OK) return rc;
-  if (use_pair(prm, nullptr, k, B, 0, N, H, D, false)) return launch_pair_noalloc(prm, stream);
   return D == 128 ? launch_noalloc<128>(prm, n_units, stream)
                   : launch_noalloc<64>(prm, n_units, stream);
 }
@@ -717,13 +584,9 @@ int attn_debug_schedule(int B, int Nq, int H, int n_key_tiles, int sms, int mask
                         const int* image_ids, int Np, int* rows, int cap, int* n_rows,
                         int* grid_out, int* slots_out) {
   if (!n_rows || !grid_out || !slots_out || (cap > 0 && !rows)) return ATTN_ERR_NULL;
-  if (B < 1 || Nq < 1 || H < 1 || sms < 1 || cap < 0 || Np < 0 || masked < 0 || masked > 2)
+  if (B < 1 || Nq < 1 || H < 1 || sms < 1 || cap < 0 || Np < 0 || masked < 0 || masked > 1)
     return ATTN_ERR_SHAPE;
-  // masked = 2: the dense family on CTA pairs (units of 512 query rows; `sms`
-  // counts pairs).
-  const bool on_pairs = masked == 2;
-  if (on_pairs) masked = 0;
-  const int unit_rows = on_pairs ? 4 * ncp::BM : 2 * ncp::BM;
+  const int unit_rows = 2 * ncp::BM;
   ncp::Params prm{};
   prm.Nq = Nq;
   prm.H = H;
@@ -784,13 +647,6 @@ int attn_debug_schedule(int B, int Nq, int H, int n_key_tiles, int sms, int mask
   *grid_out = grid;
   *slots_out = sched_slots(s);
   return count <= cap ? ATTN_OK : ATTN_ERR_SHAPE;
-}
-
-int attn_debug_set_path(int mode) {
-  if (mode < 0 || mode > 2) return ATTN_ERR_SHAPE;
-  std::lock_guard<std::mutex> lock(g_cfg_mutex);
-  g_path_mode = mode;
-  return ATTN_OK;
 }
 
 int attn_debug_set_fault(int mode, unsigned int wait_limit_us) {

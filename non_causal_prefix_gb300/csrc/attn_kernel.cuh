@@ -11,7 +11,6 @@ namespace ncp {
 constexpr int BM = 128;                  // query rows per tile (one TMEM lane each)
 constexpr int BN = 128;                  // keys per KV tile
 constexpr int NUM_THREADS = 320;
-constexpr int PAIR_THREADS = 320;        // the CTA-pair kernel
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr uint32_t TMEM_COLS = 512;
@@ -103,7 +102,7 @@ struct Sched {
   int n_units;
   int q_pairs;     // ceil(Nq / unit_rows): units per (b, h); query block fastest
   int H, Nq;
-  int unit_rows;   // query rows per unit: 256 (one CTA, two 128-row tiles) or 512 (a CTA pair)
+  int unit_rows;   // query rows per unit: two 128-row tiles
   int n_whole;     // units walked whole
   int tail_units;  // units after them, cut into key ranges (0: none)
   int tail_ctas;   // CTAs sharing the tail (0: no tail)
@@ -116,7 +115,6 @@ struct Params {
   CUtensorMap tm_q;
   CUtensorMap tm_k[2];   // [0] prefix segment, [1] current segment
   CUtensorMap tm_v[2];
-  CUtensorMap tm_kh[2];  // CTA-pair kernel: K with 64-token boxes (half a key tile per CTA)
   __nv_bfloat16* out;
   // Masked forms (block-causal, masked prefix-cached): image id per key
   // position [Np + Nq] (-1 = text) and, optionally, key_valid [B, Np + Nq]
@@ -657,12 +655,11 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, i
 // `own` takes its O from TMEM (this row's lane at o_taddr), where it still
 // is, instead of reading back its partial: the same values, 1 / nk fewer
 // bytes (called by whole warps then: the TMEM loads are warp-wide).
-template <int D, bool OWN, int SLOT_CTAS = 1>
+template <int D, bool OWN>
 __device__ __forceinline__ void merge_rows(const float4* part, int nk, uint4* dst, int own,
                                            uint32_t o_taddr) {
   constexpr int NG = D / 4 + 1;
-  // A slot holds SLOT_CTAS CTAs' partials (1; 2 for a CTA pair) of 2 tiles each.
-  const size_t piece_stride = static_cast<size_t>(2) * SLOT_CTAS * NG * BM;
+  const size_t piece_stride = static_cast<size_t>(2) * NG * BM;
   float m_all = -INFINITY;
   for (int k = 0; k < nk; ++k) m_all = fmaxf(m_all, __ldcg(part + k * piece_stride + (D / 4) * BM).x);
   float l_all = 0.f;
@@ -738,9 +735,9 @@ __device__ __forceinline__ int count_in(unsigned long long* counter, unsigned in
 
 // The merge, out of line so that its registers do not weigh on the softmax
 // loop's allocation: every piece read back from the workspace ...
-template <int D, int SLOT_CTAS = 1>
+template <int D>
 __device__ __noinline__ void merge_pieces(const float4* part, int nk, uint4* dst) {
-  merge_rows<D, false, SLOT_CTAS>(part, nk, dst, -1, 0u);
+  merge_rows<D, false>(part, nk, dst, -1, 0u);
 }
 
 // ... or, at D = 64, the merging piece's own O taken from TMEM.

@@ -303,154 +303,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       : "memory");
 }
 
-// ----------------------------------------------------------------------------
-// CTA pairs (clusters of two CTAs on an SM pair, tcgen05 cta_group::2)
-// ----------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_id_x() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t n_clusters_x() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-  return r;
-}
-// Shared-memory address `addr` of this CTA, as the same variable in CTA `rank`
-// of the cluster.
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-// Arrive on an mbarrier anywhere in the cluster (address from map_to_rank),
-// with relaxed ordering.  The arrivals hand over tensor memory (P written, O
-// read: ordered by tcgen05.wait and the tcgen05 fences) and completed copies
-// (observed on the copying CTA's own barrier), never generic stores, so they
-// need no release: a release at cluster scope costs about 1 500 cycles on
-// GB300 and put that on the softmax's critical path.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-// Test of a local mbarrier phase that acquires at cluster scope (for arrivals
-// made by the other CTA of the pair).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __noinline__ bool wait_slow_cluster(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                               volatile int* abort_flag, int site) {
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-    for (int i = 0; i < 16; ++i)
-      if (mbar_try_wait_cluster(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > limit_ns) {
-      *abort_flag = 1;
-      record_timeout(site);
-      return false;
-    }
-  }
-}
-// wait_bounded for barriers that the other CTA of the pair arrives on.
-__device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity,
-                                                     uint64_t limit_ns, volatile int* abort_flag,
-                                                     int site) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  return wait_slow_cluster(bar, parity, limit_ns, abort_flag, site);
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
-// A 32-bit word of the shared memory of another CTA of the cluster.
-__device__ __forceinline__ int ld_shared_cluster(uint32_t cluster_addr) {
-  int v;
-  asm volatile("ld.shared::cluster.b32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
-  return v;
-}
-
-// tcgen05.mma over the CTA pair (M = 256: each CTA supplies its 128 rows of A
-// and half of B's N, at the same shared-memory offsets; D lands in both CTAs'
-// tensor memory).  Issued by one thread of the even CTA.
-__device__ __forceinline__ void mma2_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma2_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Arrive on the mbarrier at `bar` (a local offset) in both CTAs of the pair
-// once every prior pair MMA of this thread has completed.
-__device__ __forceinline__ void mma2_commit_both(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-      "[%0], %1;" ::"r"(bar),
-      "h"(static_cast<unsigned short>(3))
-      : "memory");
-}
-
-// Elected forms of the pair MMAs, the pair commit and the remote arrive, for
-// loops run by whole converged warps (see mma_ss_elect).
-__device__ __forceinline__ void mma2_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                              uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma2_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                              uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma2_commit_both_elect(uint32_t bar) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-      "[%0], %1;\n\t}" ::"r"(bar),
-      "h"(static_cast<unsigned short>(3))
-      : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_cluster_elect(uint32_t cluster_addr) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-      "@e mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];\n\t}" ::"r"(cluster_addr)
-      : "memory");
-}
-// warp_wait for barriers that the other CTA of the pair arrives on.
-__device__ __forceinline__ bool warp_wait_cluster(uint32_t bar, uint32_t parity, uint64_t limit,
-                                                  volatile int* abort_flag, int site) {
-  bool ok = wait_bounded_cluster(bar, parity, limit, abort_flag, site);
-  return __all_sync(0xffffffffu, ok);
-}
-
 #define NCP_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
                   "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
 #define NCP_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), \

@@ -441,51 +441,3 @@ def test_block_causal_tail_items_stay_few():
     items = collections.Counter(int(r[0]) for r in rows if r[1] >= rounds)
     assert grid == 152 and max(items.values()) <= 3
 
-
-# The dense family on CTA pairs: units of 512 query rows, `pairs` pairs (SMs / 2).
-PAIR_CASES = [
-    # B, Nq, H, key tiles, SMs
-    (1, 4096, 32, 32, 152),    # dense N=4096: 256 units on 76 pairs
-    (1, 4096, 32, 40, 152),    # prefix 1024 + 4096
-    (1, 32768, 32, 256, 152),  # dense N=32768
-    (1, 256, 32, 256, 152),    # cross Nq=256, Nk=32768: all tail
-    (1, 8192, 32, 4, 152),     # cross Nq=8192, Nk=512
-    (1, 1000, 4, 8, 152),      # ragged
-    (3, 777, 5, 13, 14),
-    (1, 300, 1, 300, 148),
-    (2, 4096, 3, 17, 160),
-]
-
-
-def pair_sched(B, Nq, H, T, sms):
-    return ncp.debug_schedule(B, Nq, H, T, sms // 2, pairs=True)
-
-
-@pytest.mark.parametrize("B,Nq,H,T,sms", PAIR_CASES)
-def test_pair_schedule_covers_every_unit_tile_once(B, Nq, H, T, sms):
-    rows, grid, slots = pair_sched(B, Nq, H, T, sms)
-    blocks = -(-Nq // 512)
-    n_units = B * H * blocks
-    assert 1 <= grid <= sms // 2
-    seen = np.zeros((n_units, T), dtype=np.int32)
-    for pair, n, b, h, q0, two, tb, te, tail, piece, pieces, slot0 in rows:
-        assert 0 <= pair < grid and 0 <= b < B and 0 <= h < H and q0 % 512 == 0 and q0 < Nq
-        assert two == (q0 + 256 < Nq)
-        assert 0 <= tb < te <= T
-        seen[(b * H + h) * blocks + q0 // 512, tb:te] += 1
-    assert (seen == 1).all()
-    check_items_numbered(rows)
-
-
-@pytest.mark.parametrize("B,Nq,H,T,sms", PAIR_CASES)
-def test_pair_tail_fits_the_workspace(B, Nq, H, T, sms):
-    """A pair's piece takes two CTA slots ((slot0 + piece) * 2 + CTA) and a
-    tail unit four arrival counters ((tail * 2 + CTA) * 2 + tile): both must
-    stay inside the 2 x SMs of each that a workspace holds."""
-    rows, grid, slots = pair_sched(B, Nq, H, T, sms)
-    check_tail(rows, grid, slots, T, sms // 2)
-    tail = rows[rows[:, 8] >= 0]
-    if len(tail):
-        assert 2 * (int((tail[:, 11] + tail[:, 9]).max()) + 1) <= 2 * sms
-        assert 4 * (int(tail[:, 8].max()) + 1) <= 2 * sms
-    assert 2 * slots <= 2 * sms
