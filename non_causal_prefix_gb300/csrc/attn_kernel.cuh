@@ -14,9 +14,6 @@ constexpr int NUM_THREADS = 320;
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr uint32_t TMEM_COLS = 512;
-// TMEM column of S_i and O_i for query tile i.
-__host__ __device__ constexpr uint32_t tmem_s_col(int i) { return 128u * i; }
-__host__ __device__ constexpr uint32_t tmem_o_col(int i) { return 256u + 128u * i; }
 constexpr int MAX_SLOTS = 8;
 // Block-causal form: per-CTA table of the image ids in each 128-token tile
 // (min, max and "one image only"), held in shared memory; N <= 128 * this.
@@ -51,10 +48,25 @@ constexpr float RESCALE_THRESHOLD = 8.0f;
 #ifndef NCP_POLY_DEN_D64
 #define NCP_POLY_DEN_D64 4
 #endif
+// D = 64: P in TMEM columns of its own (1) or over S (0); see Cfg::P_OWN.
+#ifndef NCP_P_OWN
+#define NCP_P_OWN 1
+#endif
 
 template <int D>
 struct Cfg {
   static constexpr int CHUNKS = D / 64;                  // 128-byte swizzle columns per row
+  // TMEM columns (512) of S_i, P_i and O_i for query tile i.  D = 128: S_0,
+  // S_1, O_0, O_1 take 128 each, and P_i (bf16, two per column) is written
+  // over the first 64 columns of S_i, so S_i(j + 1) follows the P V that
+  // reads P_i(j).  D = 64: O_i takes 64 columns, which leaves 64 for each P_i
+  // (P_OWN), and S_i(j + 1) is issued as soon as P_i(j) is written, ahead of
+  // its P V: a query tile's key step is then softmax + S, not softmax + P V
+  // + S.
+  static constexpr bool P_OWN = (D == 64) && NCP_P_OWN;
+  __host__ __device__ static constexpr uint32_t s_col(int i) { return 128u * i; }
+  __host__ __device__ static constexpr uint32_t p_col(int i) { return P_OWN ? 256u + 64u * i : 128u * i; }
+  __host__ __device__ static constexpr uint32_t o_col(int i) { return P_OWN ? 384u + 64u * i : 256u + 128u * i; }
   static constexpr uint32_t TILE_BYTES = BN * D * 2;     // one K or V tile; one Q tile (BM == BN)
   static constexpr uint32_t CHUNK_BYTES = BN * 128;      // 128 rows x 128 bytes
   static constexpr int NSLOT = (D == 128) ? 4 : 8;       // K/V ring slots
@@ -86,6 +98,7 @@ struct SharedCtl {
   uint64_t p_full[2];
   uint64_t o_full[2];
   uint64_t o_free[2];
+  uint64_t pv_done[2];     // D = 64: a P V of query tile i, not an item's last, is complete
   uint64_t part_done[2];   // the 4 warps of a query tile wrote their partial rows
   uint64_t merge_ready[2]; // the piece's arrival count is known (SharedCtl::last)
   uint64_t drain;
@@ -542,12 +555,15 @@ __device__ __forceinline__ void build_row_mask(const Params& p, const RowMask& m
 }
 
 // One 128-key tile of the online softmax for this thread's query row:
-// S (fp32, TMEM) -> running max m and sum l (log2 domain) -> P (bf16) written
-// over the first 64 columns of S; O is rescaled in TMEM when m moved.
-template <int D, bool BC>
-__device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, int valid, float sl2,
-                                             bool may_rescale, const uint32_t (&vis)[4],
-                                             bool masked, float& m, float& l) {
+// S (fp32, TMEM) -> running max m and sum l (log2 domain) -> P (bf16) at
+// p_addr (64 columns); O is rescaled in TMEM when m moved.  before_store()
+// runs before P and O are written and returns false if they must not be (a
+// wait gave up); the tile then stops there and returns false.
+template <int D, bool BC, class BeforeStore>
+__device__ __forceinline__ bool softmax_tile(uint32_t s_addr, uint32_t p_addr, uint32_t o_addr,
+                                             int valid, float sl2, bool may_rescale,
+                                             const uint32_t (&vis)[4], bool masked, float& m,
+                                             float& l, BeforeStore before_store) {
   float s[BN];
   {
     uint32_t r[BN];
@@ -621,12 +637,14 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, i
     up2(acc1, a2, a3);
     l += (a0 + a1) + (a2 + a3);
   }
-  tmem_st32(s_addr + 0, pk);
-  tmem_st32(s_addr + 32, pk + 32);
+  if (!before_store()) return false;
+  tmem_st32(p_addr + 0, pk);
+  tmem_st32(p_addr + 32, pk + 32);
   if (__any_sync(0xffffffffu, rescale)) {
-    // O holds the complete sum through the previous tile: this S was issued
-    // after the previous P V and its commit has fired.  Rows of this warp
-    // that keep their maximum scale by 1.
+    // O holds the complete sum through the previous tile: D = 128, this S
+    // was issued after the previous P V and its commit has fired; D = 64,
+    // before_store() waited for that P V.  Rows of this warp that keep their
+    // maximum scale by 1.
     const uint64_t alpha2 = pk2(alpha, alpha);
 #pragma unroll
     for (int c = 0; c < D; c += 32) {
@@ -643,6 +661,7 @@ __device__ __forceinline__ void softmax_tile(uint32_t s_addr, uint32_t o_addr, i
       tmem_st32(o_addr + c, r);
     }
   }
+  return true;
 }
 
 // Merge of a tail unit's pieces for one row: `part` points at this row's
@@ -784,6 +803,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto bar_p = [&](int i) { return smem_u32(&ctl->p_full[i]); };
   auto bar_o = [&](int i) { return smem_u32(&ctl->o_full[i]); };
   auto bar_ofree = [&](int i) { return smem_u32(&ctl->o_free[i]); };
+  auto bar_pvdone = [&](int i) { return smem_u32(&ctl->pv_done[i]); };
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
@@ -797,6 +817,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(bar_p(i), 4);      // one arrival per softmax warp
       mbar_init(bar_o(i), 1);
       mbar_init(bar_ofree(i), 4);  // one arrival per softmax warp
+      mbar_init(bar_pvdone(i), 1);
       mbar_init(smem_u32(&ctl->part_done[i]), 4);
       mbar_init(smem_u32(&ctl->merge_ready[i]), 1);
     }
@@ -986,7 +1007,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-          mma_ss_elect(tmem + tmem_s_col(i), sw128_desc(qa + off, 16, 1024),
+          mma_ss_elect(tmem + C::s_col(i), sw128_desc(qa + off, 16, 1024),
                        sw128_desc(kb + off, 16, 1024), IDESC_S, kk > 0);
         }
       };
@@ -995,11 +1016,95 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t vb = ring + v_slot * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts_elect(tmem + tmem_o_col(i), tmem + tmem_s_col(i) + kk * 8,
+          mma_ts_elect(tmem + C::o_col(i), tmem + C::p_col(i) + kk * 8,
                        sw128_desc(vb + kk * 16 * 128, C::CHUNK_BYTES, 1024), IDESC_PV,
                        (accumulate || kk > 0) ? 1u : 0u);
       };
 
+      if constexpr (C::P_OWN) {
+        // D = 64, P in columns of its own.  Per visited key tile j and query
+        // tile i: once P_i(j - 1) is written, S_i(j) goes first (the softmax
+        // warps have read S_i), then P_i V(j - 1), which commits pv_done (the
+        // softmax warps wait for it before writing P_i again or rescaling
+        // O_i); an item's last P V commits o_full.  The K and V of a tile are
+        // ring loads 2 j and 2 j + 1 of the item, in load order; ld counts
+        // the loads consumed.
+        uint32_t si[2] = {0u, 0u};  // S issued per query tile (phases of s_full / p_full)
+        uint32_t oc[2] = {0u, 0u};  // items finished per query tile (phases of o_full / o_free)
+        uint32_t ld = 0;
+        bool ok = true;
+        auto ring_wait = [&](uint32_t x, int site) -> int {
+          const int sl = static_cast<int>(x % C::NSLOT);
+          if (!warp_wait(bar_kv_full(sl), (x / C::NSLOT) & 1u, limit, abort_flag, site)) return -1;
+          return sl;
+        };
+        // P_i V(j - 1): P_i(j - 1) was waited for; the first of an item waits
+        // for the epilogue that read O_i.
+        auto pv = [&](int i, int v_slot, bool accumulate) -> bool {
+          if (!accumulate && oc[i] > 0 &&
+              !warp_wait(bar_ofree(i), (oc[i] - 1u) & 1u, limit, abort_flag, 6))
+            return false;
+          tc_fence_after();
+          issue_pv(i, v_slot, accumulate);
+          return true;
+        };
+        Item it;
+        for (int n = 0; ok && (ok = await_tail(n, 13)) && get_item<BC>(p, &mtail, T, n, it); ++n) {
+          const int nq = it.u.two ? 2 : 1;
+          ok = warp_wait(bar_q, n & 1, limit, abort_flag, 2);
+          if (!ok) break;
+          int j = 0;  // key tiles visited so far in this item
+#pragma unroll 1
+          for (int t = it.t_begin; t < it.t_end && ok; ++t) {
+            if (BC && !bc_unit_visits(tt, p, it.u, t)) continue;
+            const int k_slot = ring_wait(ld, 3);
+            ok = k_slot >= 0;
+            if (!ok) break;
+            const int v_slot = j > 0 ? ring_wait(ld - 1u, 5) : 0;
+            ok = v_slot >= 0;
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              if (i >= nq || !ok) break;
+              if (j > 0) {
+                ok = warp_wait(bar_p(i), (si[i] - 1u) & 1u, limit, abort_flag, 4);
+                if (!ok) break;
+                tc_fence_after();
+              }
+              issue_s(i, k_slot);
+              mma_commit_elect(bar_s(i));
+              ++si[i];
+              if (j > 0) {
+                ok = pv(i, v_slot, j - 1 > 0);
+                if (!ok) break;
+                mma_commit_elect(bar_pvdone(i));
+              }
+            }
+            if (!ok) break;
+            mma_commit_elect(bar_kv_empty(k_slot));
+            if (j > 0) mma_commit_elect(bar_kv_empty(v_slot));
+            ld += 2u;
+            ++j;
+          }
+          if (!ok) break;
+          mma_commit_elect(bar_qfree);  // every S MMA of this item has been issued
+          const int v_slot = ring_wait(ld - 1u, 5);
+          ok = v_slot >= 0;
+          if (!ok) break;
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            if (i >= nq || !ok) break;
+            ok = warp_wait(bar_p(i), (si[i] - 1u) & 1u, limit, abort_flag, 4);
+            if (!ok) break;
+            ok = pv(i, v_slot, j - 1 > 0);
+            if (!ok) break;
+            mma_commit_elect(bar_o(i));
+            ++oc[i];
+          }
+          if (ok) mma_commit_elect(bar_kv_empty(v_slot));
+        }
+      } else {
       int slot = 0;
       uint32_t phase = 0;
       uint32_t sc[2] = {0u, 0u};  // S commits per query tile (phases of s_full / p_full)
@@ -1066,6 +1171,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (ok) mma_commit_elect(bar_kv_empty(v_prev));
       }
+      }
     }
     __syncwarp();
   } else {
@@ -1073,10 +1179,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int i = warp >> 2;  // query tile
     const int wq = warp & 3;  // TMEM lane quarter
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t s_addr = tmem + lane_base + tmem_s_col(i);
-    const uint32_t o_addr = tmem + lane_base + tmem_o_col(i);
+    const uint32_t s_addr = tmem + lane_base + C::s_col(i);
+    const uint32_t p_addr = tmem + lane_base + C::p_col(i);
+    const uint32_t o_addr = tmem + lane_base + C::o_col(i);
     const float sl2 = p.scale_log2;
     uint32_t sc = 0, oc = 0;  // phases of s_full / p_full and of o_full / o_free
+    uint32_t pvc = 0;         // D = 64: phases of pv_done waited
     bool ok = true;
     uint32_t mc = 0;  // split items done by this query tile (phases of part_done / merge_ready)
     const uint32_t bar_part = smem_u32(&ctl->part_done[i]);
@@ -1181,8 +1289,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // scores must be -inf instead.
         const int seg = (t < T0) ? 0 : 1;
         const int valid = p.n_tok[seg] - (t - (seg ? T0 : 0)) * BN;
-        softmax_tile<D, BC>(s_addr, o_addr, valid, sl2, j > 0, vis, masked, m, l);
+        // D = 64: P_i and O_i may be written once the previous P V is complete
+        // (an item's first tile: the previous item's last P V, which its
+        // epilogue waited for).
+        const bool first = j == 0;
+        auto before_store = [&]() -> bool {
+          if constexpr (C::P_OWN) {
+            if (!first) {
+              if (!warp_wait(bar_pvdone(i), pvc & 1u, limit, abort_flag, 15)) return false;
+              ++pvc;
+              tc_fence_after();
+            }
+          }
+          return true;
+        };
+        ok = softmax_tile<D, BC>(s_addr, p_addr, o_addr, valid, sl2, !first, vis, masked, m, l,
+                                 before_store);
         ++j;
+        if (!ok) break;
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
