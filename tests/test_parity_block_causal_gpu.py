@@ -6,6 +6,8 @@ image runs that start and end inside 128-token tiles, an id reused by two
 separate blocks (outside the definition's contiguity promise: the kernel is
 exact for any ids), single tokens and a one-token sequence.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -54,6 +56,18 @@ def test_block_causal_small(cuda_lib, oracle_mod, case):
 def test_block_causal_workload(cuda_lib, oracle_mod):
     w = workloads.WORKLOADS[6]
     ins, ids, out = run(cuda_lib, w, None)
+    ref = oracle_mod.block_causal_attention(*bits(ins), ids.numpy())
+    s = assert_parity(out.float().cpu().numpy().astype(np.float64), ref, w.describe())
+    print(w.name, s)
+
+
+def test_block_causal_workload_d64(cuda_lib, oracle_mod):
+    """The workload's ids at D = 64, where P has TMEM columns of its own and
+    the next S goes out ahead of the P V: 32 heads give each CTA several work
+    items and a split tail, so the per-tile barrier phases carry across items."""
+    w6 = workloads.WORKLOADS[6]
+    w = dataclasses.replace(w6, D=64, name=w6.name.replace("d128", "d64"))
+    ins, ids, out = run(cuda_lib, w, 12900)
     ref = oracle_mod.block_causal_attention(*bits(ins), ids.numpy())
     s = assert_parity(out.float().cpu().numpy().astype(np.float64), ref, w.describe())
     print(w.name, s)

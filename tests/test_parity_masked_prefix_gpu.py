@@ -5,6 +5,8 @@ key_valid[b, j]; runtime sm_scale) against the FP64 oracle, through the C ABI.
 Cases cover an empty prefix, prefixes whose length is not a multiple of 4
 (unaligned id loads) or of 128 (tiles straddling the segment boundary),
 per-batch key padding and D = 64."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -61,6 +63,19 @@ def test_masked_prefix_small(cuda_lib, oracle_mod, case):
 def test_masked_prefix_workload(cuda_lib, oracle_mod):
     w = workloads.WORKLOADS[9]
     q, kc, vc, kp, vp = workloads.make_inputs(w)
+    ids, valid = workloads.image_ids(w), workloads.key_valid(w)
+    out = gpu(cuda_lib, q, kc, vc, kp, vp, ids, valid, w.sm_scale)
+    ref = oracle_of(oracle_mod, q, kc, vc, kp, vp, ids, valid, float(np.float32(w.sm_scale)))
+    s = assert_parity(out.float().cpu().numpy().astype(np.float64), ref, w.describe())
+    print(w.name, s)
+
+
+def test_masked_prefix_workload_d64(cuda_lib, oracle_mod):
+    """The workload's prefix, ids and padding at D = 64 (scale 1/8), where P
+    has TMEM columns of its own and the next S goes out ahead of the P V."""
+    w9 = workloads.WORKLOADS[9]
+    w = dataclasses.replace(w9, D=64, sm_scale=0.125, name=w9.name.replace("d128", "d64"))
+    q, kc, vc, kp, vp = workloads.make_inputs(w, seed_base=15900)
     ids, valid = workloads.image_ids(w), workloads.key_valid(w)
     out = gpu(cuda_lib, q, kc, vc, kp, vp, ids, valid, w.sm_scale)
     ref = oracle_of(oracle_mod, q, kc, vc, kp, vp, ids, valid, float(np.float32(w.sm_scale)))
