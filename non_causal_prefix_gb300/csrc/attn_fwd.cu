@@ -619,7 +619,7 @@ int attn_debug_schedule(int B, int Nq, int H, int n_key_tiles, int sms, int mask
     int* cnt = order.data() + ncp::ORDER_QP + ncp::MAX_Q_PAIRS;
     for (int q = 0; q < s.q_pairs; ++q) {
       ncp::Unit uq{0, 0, q * 2 * ncp::BM, q * 2 * ncp::BM + ncp::BM < Nq};
-      for (int t = 0; t < T; ++t) cnt[q] += ncp::bc_unit_visits(mt.tt, prm, uq, t) ? 1 : 0;
+      for (int t = 0; t < T; ++t) cnt[q] += ncp::bc_pair_tile_cost(mt.tt, prm, uq, t);
     }
     for (int q = 0; q < s.q_pairs; ++q)
       order[ncp::ORDER_QP + ncp::order_rank(cnt, s.q_pairs, q)] = q;

@@ -157,10 +157,10 @@ struct Unit {
   bool two;  // the second 128-row query tile has at least one row
 };
 
-// Masked forms: the order of the units.  A unit's work is the number of key
-// tiles its query pair visits (the same for every batch and head), so the
-// query pairs are sorted by that count, most first (ties: the later pair
-// first); pairs of one count form a level.  Units go level by level, and
+// Masked forms: the order of the units.  A unit's work depends only on its
+// query pair (the same for every batch and head): its cost, bc_pair_tile_cost
+// summed over the key tiles, orders the query pairs, most first (ties: the
+// later pair first); pairs of one cost form a level.  Units go level by level, and
 // within a level head-major with the query pair fastest, as in the dense
 // order, so that the CTAs running at one time share few heads' K/V in L2.
 // Tables (int block): [0] number of levels L, [1 .. L + 1] first index into
@@ -271,11 +271,28 @@ __host__ __device__ __forceinline__ bool bc_unit_visits(const TileTable& tt, con
 // q_first) sees every key of tile t through causality or one shared image
 // (key_valid aside): the keys all precede the rows, or both tiles hold one
 // and the same image.
-__device__ __forceinline__ bool bc_tile_full(const TileTable& tt, const Params& p, int qt,
-                                             int q_first, int t) {
+__host__ __device__ __forceinline__ bool bc_tile_full(const TileTable& tt, const Params& p,
+                                                      int qt, int q_first, int t) {
   if (key_tile_pos(p, t) + key_tile_len(p, t) - 1 <= p.n_tok[0] + q_first) return true;
   const int tq = p.n_tiles[0] + qt;
   return tt.uni(tq) && tt.uni(t) && tt.lo(tq) == tt.lo(t);
+}
+
+// Cost of key tile t to the query pair of unit u (masked forms), in units of
+// about 1/16 us of a GB300 CTA: 0 if no row of the pair sees the tile, else
+// 26 for a pair of two query tiles or 22 for one (one tile loses the other's
+// overlap), plus 6 for each query tile that sees only part of the key tile
+// (it builds a row mask).  Fitted to the per-CTA times of a traced
+// block-causal launch: 1.62, 1.38 and 0.35 us.  Only the order of the units
+// uses it.
+__host__ __device__ __forceinline__ int bc_pair_tile_cost(const TileTable& tt, const Params& p,
+                                                          const Unit& u, int t) {
+  if (!bc_unit_visits(tt, p, u, t)) return 0;
+  const int qt0 = u.q0 / BM;
+  int c = u.two ? 26 : 22;
+  if (!bc_tile_full(tt, p, qt0, u.q0, t)) c += 6;
+  if (u.two && !bc_tile_full(tt, p, qt0 + 1, u.q0 + BM, t)) c += 6;
+  return c;
 }
 
 // Owner of tail position x (tail positions in unit order): CTA c of G holds
@@ -905,7 +922,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uq.h = 0;
       uq.q0 = q * 2 * BM;
       uq.two = uq.q0 + BM < p.Nq;
-      if (bc_unit_visits(tt, p, uq, t)) atomicAdd(&cnt[q], 1);
+      const int cost = bc_pair_tile_cost(tt, p, uq, t);
+      if (cost) atomicAdd(&cnt[q], cost);
     }
     __syncthreads();
     for (int q = threadIdx.x; q < qpn; q += NUM_THREADS) ob[ORDER_QP + order_rank(cnt, qpn, q)] = q;

@@ -294,13 +294,42 @@ def visited_per_pair(ids, Np, Nq):
     return counts
 
 
+def pair_costs(ids, Np, Nq):
+    """Cost of each query pair's unit, restated: per visited key tile, 26 when
+    the pair has two query tiles and 22 when it has one, plus 6 for each of its
+    query tiles that sees only part of the key tile.  A query tile sees all of
+    a key tile when the tile's last key is at or before the query tile's first
+    position, or when both tiles hold one and the same image (no text)."""
+    T0, T1 = -(-Np // 128), -(-Nq // 128)
+    pos0 = [t * 128 if t < T0 else Np + (t - T0) * 128 for t in range(T0 + T1)]
+    ln = [min(128, (Np if t < T0 else Nq) - (t if t < T0 else t - T0) * 128) for t in range(T0 + T1)]
+    one_image = []
+    for t in range(T0 + T1):
+        seg = ids[pos0[t]:pos0[t] + ln[t]]
+        one_image.append(int(seg[0]) if (seg >= 0).all() and (seg == seg[0]).all() else None)
+    costs = []
+    for q in range(-(-Nq // 256)):
+        two = q * 256 + 128 < Nq
+        c = 0
+        for t in visited_tiles(ids, Np, Nq, q):
+            c += 26 if two else 22
+            for qt in range(2 if two else 1):
+                first = Np + q * 256 + qt * 128
+                tq = T0 + 2 * q + qt
+                full = (pos0[t] + ln[t] - 1 <= first or
+                        (one_image[tq] is not None and one_image[tq] == one_image[t]))
+                c += 0 if full else 6
+        costs.append(c)
+    return costs
+
+
 @pytest.mark.parametrize("B,Nq,H,Np,segments,sms", MASKED)
 def test_masked_forms_deal_a_snake(B, Nq, H, Np, segments, sms):
-    """Whole masked units: query pairs sorted by the key tiles they visit (most
+    """Whole masked units: query pairs sorted by their cost (pair_costs; most
     first, the later pair first among equals); units level by level, head-major
     with the query pair fastest within a level; dealt in a snake."""
     (rows, grid, _), ids = masked_sched(B, Nq, H, Np, segments, sms)
-    cnt = visited_per_pair(ids, Np, Nq)
+    cnt = pair_costs(ids, Np, Nq)
     q_pairs = len(cnt)
     n_bh = B * H
     order = sorted(range(q_pairs), key=lambda q: (-cnt[q], -q))
@@ -371,8 +400,9 @@ def check_masked_tail_layout(B, Nq, H, Np, segments, sms):
     tail_rows = [r for r in rows if r[1] >= n_units // grid] if rem and g_tail > rem else []
     if not tail_rows:
         return
-    order = sorted(range(q_pairs), key=lambda q: (-cnt[q], -q))
-    levels = [r for r in range(q_pairs) if r == 0 or cnt[order[r]] != cnt[order[r - 1]]]
+    cost = pair_costs(ids, Np, Nq)
+    order = sorted(range(q_pairs), key=lambda q: (-cost[q], -q))
+    levels = [r for r in range(q_pairs) if r == 0 or cost[order[r]] != cost[order[r - 1]]]
     levels.append(q_pairs)
 
     def unit_pair(u):
