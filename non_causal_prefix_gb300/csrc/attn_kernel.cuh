@@ -1412,21 +1412,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         continue;
       }
 
-      // A whole unit: O / l -> bf16 -> this thread's output row.
+      // A whole unit: O / l -> bf16 -> this thread's output row, in 32-byte
+      // stores when the output is 32-byte aligned (rows are D * 2 bytes apart),
+      // else in 16-byte ones.  The rows of a warp are H * D * 2 bytes apart, so
+      // every store of the warp writes 32 separate sectors; whole sectors
+      // halve the write requests at the end of each work item.
       if (q < p.Nq) {
         const float inv_l = 1.f / l;
         const uint64_t inv2 = pk2(inv_l, inv_l);
+        if ((reinterpret_cast<uintptr_t>(p.out) & 31u) == 0) {
 #pragma unroll
-        for (int c = 0; c < D; c += 8) {
-          uint32_t w[4];
+          for (int c = 0; c < D; c += 16) {
+            uint32_t w[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float a0, a1;
-            up2(fmul2(pk2(__uint_as_float(r[c + 2 * e]), __uint_as_float(r[c + 2 * e + 1])), inv2),
-                a0, a1);
-            w[e] = pack_bf16x2(a0, a1);
+            for (int e = 0; e < 8; ++e) {
+              float a0, a1;
+              up2(fmul2(pk2(__uint_as_float(r[c + 2 * e]), __uint_as_float(r[c + 2 * e + 1])), inv2),
+                  a0, a1);
+              w[e] = pack_bf16x2(a0, a1);
+            }
+            st_global_v8(dst + c / 8, w);
           }
-          dst[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < D; c += 8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              float a0, a1;
+              up2(fmul2(pk2(__uint_as_float(r[c + 2 * e]), __uint_as_float(r[c + 2 * e + 1])), inv2),
+                  a0, a1);
+              w[e] = pack_bf16x2(a0, a1);
+            }
+            dst[c / 8] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
         }
       }
     }

@@ -145,6 +145,14 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// A 32-byte store (address 32-byte aligned): a whole sector per lane, half
+// the write requests of two 16-byte stores.
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t (&w)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // Two fp32 values in one 64-bit register pair, for the packed f32x2 ALU ops.
 __device__ __forceinline__ uint64_t pk2(float lo, float hi) {
   uint64_t r;

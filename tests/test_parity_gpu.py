@@ -223,6 +223,31 @@ def test_timeout_in_split_launch_leaves_next_call_exact(cuda_lib, oracle_mod):
     assert_parity(f64(out).reshape(-1, w.D)[rows], ref, "after a split-launch timeout")
 
 
+@pytest.mark.parametrize("B,N,H,D", [(1, 1000, 2, 128), (2, 300, 3, 64), (1, 4096, 32, 128)])
+def test_output_aligned_16_not_32(cuda_lib, oracle_mod, B, N, H, D):
+    """An output 16 bytes past a 32-byte boundary (the entry points ask for 16)
+    takes the 16-byte stores: bit-identical to an aligned output, and exact
+    against the oracle.  The last shape splits units across SMs, so the
+    merge's writes are covered too."""
+    w = workloads.custom("dense", B, N, N, H, D)
+    ins = workloads.make_inputs(w, seed_base=7600 + N + D)
+    q, k, v = to_dev(ins)
+    ref_out = gpu_dense(cuda_lib, q, k, v)
+    assert ref_out.data_ptr() % 32 == 0
+    buf = torch.empty(q.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    out = buf[8:].view(q.shape)
+    assert out.data_ptr() % 32 == 16
+    cuda_lib.attn_dense_fwd(q, k, v, out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_out)
+    if N * H <= 2000:
+        assert_parity(f64(out), oracle_mod.dense_attention(*bits(ins)), w.describe())
+    else:
+        rows = sample_rows(B, N, H, 60, seed=7601)
+        ref = oracle_mod.dense_attention_rows(*bits(ins), rows)
+        assert_parity(f64(out).reshape(-1, D)[rows], ref, w.describe())
+
+
 def test_binding_rejects_bad_tensors(cuda_lib):
     q = torch.zeros(1, 128, 2, 64, device="cuda", dtype=torch.bfloat16)
     with pytest.raises(TypeError):
