@@ -103,11 +103,17 @@ struct SharedCtl {
   uint64_t merge_ready[2]; // the piece's arrival count is known (SharedCtl::last)
   uint64_t drain;
   uint64_t tail_ready;     // masked forms: this CTA's tail items are in shared memory
+  uint64_t item_full[2];   // the loader has written work item slot s (item n: slot n & 1)
+  uint64_t item_empty[2];  // the 8 softmax warps and the MMA warp have read slot s
   int last[2];             // this piece is the last of its unit: merge and store
   int n_tail_items;        // masked forms: tail items of this CTA kept in shared memory
   uint32_t tmem_base;
   int abort_flag;
+  // Work items as the loader decoded them, two slots (an Item, 48 bytes at
+  // most): the other roles read them instead of decoding each item again.
+  alignas(16) unsigned char item_ring[2][48];
 };
+static_assert(sizeof(SharedCtl) <= 512, "the barrier block holds 512 bytes");
 
 // Work schedule of one launch.  Units are (b, h, pair of 128-row query
 // tiles), n_units = B * H * q_pairs of them; see schedule_item.
@@ -820,6 +826,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto bar_p = [&](int i) { return smem_u32(&ctl->p_full[i]); };
   auto bar_o = [&](int i) { return smem_u32(&ctl->o_full[i]); };
   auto bar_ofree = [&](int i) { return smem_u32(&ctl->o_free[i]); };
+  auto bar_ifull = [&](int s) { return smem_u32(&ctl->item_full[s]); };
+  auto bar_iempty = [&](int s) { return smem_u32(&ctl->item_empty[s]); };
+  Item* const item_ring = reinterpret_cast<Item*>(ctl->item_ring);
   auto bar_pvdone = [&](int i) { return smem_u32(&ctl->pv_done[i]); };
 
   if (threadIdx.x == 0) {
@@ -840,6 +849,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     mbar_init(smem_u32(&ctl->drain), 1);
     mbar_init(smem_u32(&ctl->tail_ready), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar_ifull(s), 1);
+      mbar_init(bar_iempty(s), NUM_THREADS / 32 - 1);  // every warp but the loader
+    }
     ctl->n_tail_items = MAX_CTA_TAIL_ITEMS;
     ctl->abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -949,6 +962,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mtail.n_items = ctl->n_tail_items;
     return true;
   };
+  // Work item n, decoded once by the loader and read by the other roles
+  // (whole warps).  The loader writes item n into slot n & 1 once every
+  // reader has taken item n - 2 (item_empty), then arrives on item_full; a
+  // slot with t_begin < 0 means no item is left.  take_item returns false at
+  // the end or, with ok false, when a wait gave up.
+  auto publish_item = [&](int n, const Item* src) -> bool {
+    const int sl = n & 1;
+    if (n >= 2 && !warp_wait(bar_iempty(sl), ((n >> 1) - 1) & 1, limit, abort_flag, 17))
+      return false;
+    if (lane == 0) {
+      if (src) item_ring[sl] = *src; else item_ring[sl].t_begin = -1;
+      mbar_arrive(bar_ifull(sl));
+    }
+    __syncwarp();
+    return true;
+  };
+  auto take_item = [&](int n, Item& out, bool& ok) -> bool {
+    const int sl = n & 1;
+    ok = warp_wait(bar_ifull(sl), (n >> 1) & 1, limit, abort_flag, 16);
+    if (!ok) return false;
+    out = item_ring[sl];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_iempty(sl));
+    return out.t_begin >= 0;
+  };
   // Loader bookkeeping for draining copies in flight after an abort.
   uint32_t ld_issued = 0, ld_parity = 0;  // per ring slot: a load was issued / its phase
   int q_last = -1;                        // last unit whose Q load was issued
@@ -970,7 +1008,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       bool ok = true;
       Item it;
-      for (int n = 0; ok && (ok = await_tail(n, 12)) && get_item<BC>(p, &mtail, T, n, it); ++n) {
+      for (int n = 0; ok; ++n) {
+        ok = await_tail(n, 12);
+        if (!ok) break;
+        const bool has = get_item<BC>(p, &mtail, T, n, it);
+        ok = publish_item(n, has ? &it : nullptr);
+        if (!ok || !has) break;
         const Unit& u = it.u;
         // The Q buffers are free once every S MMA of the previous item is done.
         if (n > 0) {
@@ -1067,7 +1110,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           return true;
         };
         Item it;
-        for (int n = 0; ok && (ok = await_tail(n, 13)) && get_item<BC>(p, &mtail, T, n, it); ++n) {
+        for (int n = 0; ok && take_item(n, it, ok); ++n) {
           const int nq = it.u.two ? 2 : 1;
           ok = warp_wait(bar_q, n & 1, limit, abort_flag, 2);
           if (!ok) break;
@@ -1140,7 +1183,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         return true;
       };
       Item it;
-      for (int n = 0; ok && (ok = await_tail(n, 13)) && get_item<BC>(p, &mtail, T, n, it); ++n) {
+      for (int n = 0; ok && take_item(n, it, ok); ++n) {
         const int nq = it.u.two ? 2 : 1;
         ok = warp_wait(bar_q, n & 1, limit, abort_flag, 2);
         if (!ok) break;
@@ -1275,7 +1318,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mtail.n_items = ctl->n_tail_items;
     }
     Item it;
-    for (int n = 0; ok && get_item<BC>(p, &mtail, T, n, it); ++n) {
+    for (int n = 0; ok && take_item(n, it, ok); ++n) {
       const Unit& u = it.u;
       if (i == 1 && !u.two) continue;
       float m = -INFINITY;  // running (possibly stale) maximum, log2 units
