@@ -281,6 +281,33 @@ def time_device(torch, call, flush, steps, warmup, stream):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)], (t0, t1)
 
 
+def time_graph(torch, call, stream, iters, reps=5):
+    """Per-launch device time (ms) of `iters` back-to-back launches captured in
+    one CUDA graph on `stream` and replayed: the median over `reps` replays,
+    timed with CUDA events on that stream.  No L2 flush runs between the
+    launches, so inputs that fit in L2 stay there (warm timing)."""
+    call(stream)  # a splitting call captures the workspace its stream used last
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(iters):
+            call(stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) / iters)
+    del g
+    return statistics.median(ts)
+
+
 def time_e2e(torch, ncp, w, host_in, steps, warmup, stream):
     """Host-to-host time per step through the C-ABI call: every step copies its
     inputs in from pinned host memory, runs the call and copies the output back
@@ -493,7 +520,10 @@ def run_gpu(args):
 
 
 def per_config(torch, ncp, flush, stream, peak, args):
-    """Device TFLOP/s of every synthetic workload (context for the line)."""
+    """Device TFLOP/s of every synthetic workload (context for the line): the
+    median, mean and min of per-launch CUDA-event times with the L2 flushed
+    before each launch, and graph_us, the per-launch time of graph_iters
+    back-to-back launches replayed from one CUDA graph (warm L2)."""
     res = {}
     for cid, w in workloads.WORKLOADS.items():
         dev_in = [t.cuda() for t in workloads.make_inputs(w)]
@@ -503,8 +533,12 @@ def per_config(torch, ncp, flush, stream, peak, args):
         times, _ = time_device(torch, call, flush, steps, 3, stream)
         us = statistics.median(times) * 1e3
         tf = w.flops / (us / 1e6) / 1e12
+        iters = max(1, min(50, int(2000.0 / us)))
+        g_us = time_graph(torch, call, stream, iters) * 1e3
         res[w.name] = {"median_us": round(us, 2), "mean_us": round(statistics.mean(times) * 1e3, 2),
+                       "min_us": round(min(times) * 1e3, 2),
                        "tflops": round(tf, 1), "frac_of_peak": round(tf / peak, 4),
+                       "graph_us": round(g_us, 2), "graph_iters": iters,
                        "tensor_pipe_active_pct": recorded_profile(w.name).get(
                            "tensor_pipe_active_pct")}
         del dev_in, out
