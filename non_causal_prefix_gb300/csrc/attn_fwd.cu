@@ -115,9 +115,14 @@ bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) !
 // Cost of one extra tail piece on a CTA, in key-tile times: its Q load and
 // pipeline fill, its partial written and counted in, and the merge.  On
 // GB300 a CTA with two tail pieces ends about 6 tiles after one with a single
-// piece of the same length, but part of that overlaps; of the costs 1, 2, 3,
-// 5 and 8 tried, 3 gave the shortest launches.
-constexpr long long PIECE_COST = 3;
+// piece of the same length, but part of that overlaps.  Of the costs 1, 2, 3,
+// 5 and 8 tried, 3 gave the shortest launches.  (Re-measured with 2, 3, 4 and
+// 6: 4 was up to 1.6 % faster on the split workloads, but on short key
+// sequences it stops splitting tails that 3 still splits.)
+#ifndef NCP_PIECE_COST
+#define NCP_PIECE_COST 3
+#endif
+constexpr long long PIECE_COST = NCP_PIECE_COST;
 
 // Dense tail ranges: cut W tail tiles (units of T tiles, in order) into
 // consecutive non-empty ranges, each CTA's tiles plus PIECE_COST for every
