@@ -951,11 +951,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  // Masked forms with a split tail: the first tail item of a CTA's loader and
-  // MMA issuer waits until the softmax warps have worked the tail items out.
+  // Masked forms with a split tail: the loader, which decodes every work item
+  // for the other roles, waits before its first tail item until the softmax
+  // warps have worked the tail items out.
   const int tail_rounds = p.sc.tail_ctas ? p.sc.n_whole / static_cast<int>(gridDim.x) : 0;
   const uint32_t bar_tail = smem_u32(&ctl->tail_ready);
-  // (Called by the loader and the MMA issuer, whole warps.)
+  // (Called by the loader, whole warp.)
   auto await_tail = [&](int n, int site) -> bool {
     if (!masked_tail || n < tail_rounds || mtail.n_items > 0) return true;
     if (!warp_wait(bar_tail, 0, limit, abort_flag, site)) return false;
