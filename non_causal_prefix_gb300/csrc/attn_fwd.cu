@@ -330,7 +330,7 @@ int launch(Params& prm, long long n_units, cudaStream_t stream) {
   prm.ws_count = nullptr;
   prm.epoch = 1;
   if (prm.sc.tail_ctas == 0) {
-    ncp::attn_fwd_kernel<D, BC><<<grid, ncp::NUM_THREADS, smem, stream>>>(prm);
+    ncp::attn_fwd_kernel<D, BC><<<grid, ncp::num_threads<D>(), smem, stream>>>(prm);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
   }
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
@@ -343,13 +343,13 @@ int launch(Params& prm, long long n_units, cudaStream_t stream) {
   Workspace* ws = take_workspace(dev, sms, stream, capturing);
   if (!ws) {
     grid = make_sched(prm.sc, n_units, T, sms, false, BC);
-    ncp::attn_fwd_kernel<D, BC><<<grid, ncp::NUM_THREADS, smem, stream>>>(prm);
+    ncp::attn_fwd_kernel<D, BC><<<grid, ncp::num_threads<D>(), smem, stream>>>(prm);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
   }
   prm.ws_part = ws->part;
   prm.ws_count = ws->count;
   prm.epoch = next_epoch(*ws);
-  ncp::attn_fwd_kernel<D, BC><<<grid, ncp::NUM_THREADS, smem, stream>>>(prm);
+  ncp::attn_fwd_kernel<D, BC><<<grid, ncp::num_threads<D>(), smem, stream>>>(prm);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   ws->last_stream = reinterpret_cast<uintptr_t>(stream);
   if (!capturing && cudaEventRecord(ws->done, stream) != cudaSuccess) {
@@ -460,7 +460,7 @@ int launch_noalloc(Params& prm, long long n_units, cudaStream_t stream) {
   prm.epoch = 1;  // the counters were just cleared (tag 0)
   prm.ws_part = reinterpret_cast<float*>(static_cast<unsigned char*>(scratch) +
                                          ncp::NOALLOC_COUNT_BYTES);
-  ncp::attn_fwd_kernel<D, false><<<grid, ncp::NUM_THREADS, C::SMEM_BYTES, stream>>>(prm);
+  ncp::attn_fwd_kernel<D, false><<<grid, ncp::num_threads<D>(), C::SMEM_BYTES, stream>>>(prm);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

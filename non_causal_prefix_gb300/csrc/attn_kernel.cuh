@@ -10,9 +10,11 @@ namespace ncp {
 
 constexpr int BM = 128;                  // query rows per tile (one TMEM lane each)
 constexpr int BN = 128;                  // keys per KV tile
-constexpr int NUM_THREADS = 320;
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;
+// D = 64 (P in TMEM columns of its own): a second MMA warp issues query tile
+// 1's MMAs, so that neither tile's next S waits behind the other's P V.
+constexpr int MMA_WARP2 = 10;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int MAX_SLOTS = 8;
 // Block-causal form: per-CTA table of the image ids in each 128-token tile
@@ -88,6 +90,13 @@ struct Cfg {
   static_assert(POLY_DEN >= 1 && POLY_NUM >= 0 && POLY_NUM <= POLY_DEN, "polynomial share");
   __host__ __device__ static constexpr bool poly_pair(int c) { return (c % POLY_DEN) >= POLY_DEN - POLY_NUM; }
 };
+
+// Threads of a CTA: 10 warps (8 softmax, the loader, the MMA warp), plus the
+// second MMA warp where P has columns of its own.
+template <int D>
+__host__ __device__ constexpr int num_threads() {
+  return Cfg<D>::P_OWN ? 352 : 320;
+}
 
 struct SharedCtl {
   uint64_t q_full;
@@ -795,11 +804,13 @@ __device__ __noinline__ void merge_pieces_own(const float4* part, int nk, uint4*
 // BC = false: dense and prefix-cached forms (every key visible).
 // BC = true: block-causal form (one key segment, per-row image-id mask).
 template <int D, bool BC>
-// 10 warps on 4 SM sub-partitions (16 Ki registers each, 3 warps on two of
-// them) cap a thread at 168 registers.
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+// 10 or 11 warps on 4 SM sub-partitions (16 Ki registers each, 3 warps on
+// two or three of them) cap a thread at 168 registers.
+__global__ void __launch_bounds__(num_threads<D>(), 1)
     attn_fwd_kernel(const __grid_constant__ Params p) {
   using C = Cfg<D>;
+  constexpr int NT = num_threads<D>();
+  constexpr bool DUAL = C::P_OWN;  // two MMA warps, one per query tile
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte swizzle atoms.
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -833,10 +844,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    mbar_init(bar_qfree, 1);
+    mbar_init(bar_qfree, DUAL ? 2 : 1);  // one release per MMA warp
     for (int s = 0; s < C::NSLOT; ++s) {
       mbar_init(bar_kv_full(s), 1);
-      mbar_init(bar_kv_empty(s), 1);
+      mbar_init(bar_kv_empty(s), DUAL ? 2 : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_s(i), 1);
@@ -847,11 +858,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(smem_u32(&ctl->part_done[i]), 4);
       mbar_init(smem_u32(&ctl->merge_ready[i]), 1);
     }
-    mbar_init(smem_u32(&ctl->drain), 1);
+    mbar_init(smem_u32(&ctl->drain), DUAL ? 2 : 1);
     mbar_init(smem_u32(&ctl->tail_ready), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar_ifull(s), 1);
-      mbar_init(bar_iempty(s), NUM_THREADS / 32 - 1);  // every warp but the loader
+      mbar_init(bar_iempty(s), NT / 32 - 1);  // every warp but the loader
     }
     ctl->n_tail_items = MAX_CTA_TAIL_ITEMS;
     ctl->abort_flag = 0;
@@ -872,7 +883,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // 16-byte aligned (image_ids itself is).
   TileTable tt{nullptr};
   if constexpr (BC) {
-    constexpr int NW = NUM_THREADS / 32;
+    constexpr int NW = NT / 32;
     int* t_lo = reinterpret_cast<int*>(base + C::SUM_OFF);
     for (int t0 = warp; t0 < T; t0 += 4 * NW) {
       int id[4][4];
@@ -926,9 +937,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int* ob = reinterpret_cast<int*>(base + C::ORDER_OFF);
     int* cnt = ob + ORDER_QP + MAX_Q_PAIRS;
     const int qpn = p.sc.q_pairs;
-    for (int q = threadIdx.x; q < qpn; q += NUM_THREADS) cnt[q] = 0;
+    for (int q = threadIdx.x; q < qpn; q += NT) cnt[q] = 0;
     __syncthreads();
-    for (int x = threadIdx.x; x < qpn * T; x += NUM_THREADS) {
+    for (int x = threadIdx.x; x < qpn * T; x += NT) {
       const int q = x / T, t = x - q * T;
       Unit uq;
       uq.b = 0;
@@ -939,7 +950,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (cost) atomicAdd(&cnt[q], cost);
     }
     __syncthreads();
-    for (int q = threadIdx.x; q < qpn; q += NUM_THREADS) ob[ORDER_QP + order_rank(cnt, qpn, q)] = q;
+    for (int q = threadIdx.x; q < qpn; q += NT) ob[ORDER_QP + order_rank(cnt, qpn, q)] = q;
     __syncthreads();
     if (threadIdx.x == 0) order_levels(ob, cnt, qpn);
   }
@@ -1055,8 +1066,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     __syncwarp();
-  } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == MMA_WARP || (DUAL && warp == MMA_WARP2)) {
+    // ----------------------------------------------------------- MMA issuers
     // The whole warp runs the loop, converged (warp-wide bounded waits); one
     // elected lane issues each MMA and commit (see mma_ss_elect).
     {
@@ -1084,15 +1095,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       };
 
       if constexpr (C::P_OWN) {
-        // D = 64, P in columns of its own.  Per visited key tile j and query
-        // tile i: once P_i(j - 1) is written, S_i(j) goes first (the softmax
-        // warps have read S_i), then P_i V(j - 1), which commits pv_done (the
-        // softmax warps wait for it before writing P_i again or rescaling
-        // O_i); an item's last P V commits o_full.  The K and V of a tile are
-        // ring loads 2 j and 2 j + 1 of the item, in load order; ld counts
-        // the loads consumed.
-        uint32_t si[2] = {0u, 0u};  // S issued per query tile (phases of s_full / p_full)
-        uint32_t oc[2] = {0u, 0u};  // items finished per query tile (phases of o_full / o_free)
+        // D = 64, P in columns of its own; one MMA warp per query tile i.
+        // Per visited key tile j: once P_i(j - 1) is written, S_i(j) goes
+        // first (the softmax warps have read S_i), then P_i V(j - 1), which
+        // commits pv_done (the softmax warps wait for it before writing P_i
+        // again or rescaling O_i); an item's last P V commits o_full.  The K
+        // and V of a tile are ring loads 2 j and 2 j + 1 of the item, in load
+        // order; ld counts the loads consumed.  A ring slot and the Q buffers
+        // are free once both warps have released them (kv_empty and q_free
+        // take two arrivals): by a commit after their MMAs, or, for an item
+        // without this warp's query tile, by a plain arrival made after the
+        // slot's or Q's full phase, so that it never counts toward the phase
+        // before.
+        const int i = warp - MMA_WARP;  // this warp's query tile
+        uint32_t si = 0;  // S issued (phases of s_full / p_full)
+        uint32_t oc = 0;  // items finished (phases of o_full / o_free)
         uint32_t ld = 0;
         bool ok = true;
         auto ring_wait = [&](uint32_t x, int site) -> int {
@@ -1100,11 +1117,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!warp_wait(bar_kv_full(sl), (x / C::NSLOT) & 1u, limit, abort_flag, site)) return -1;
           return sl;
         };
+        auto release = [&](uint32_t bar, bool mine) {
+          if (mine) {
+            mma_commit_elect(bar);
+          } else {
+            if (lane == 0) mbar_arrive(bar);
+            __syncwarp();
+          }
+        };
         // P_i V(j - 1): P_i(j - 1) was waited for; the first of an item waits
         // for the epilogue that read O_i.
-        auto pv = [&](int i, int v_slot, bool accumulate) -> bool {
-          if (!accumulate && oc[i] > 0 &&
-              !warp_wait(bar_ofree(i), (oc[i] - 1u) & 1u, limit, abort_flag, 6))
+        auto pv = [&](int v_slot, bool accumulate) -> bool {
+          if (!accumulate && oc > 0 &&
+              !warp_wait(bar_ofree(i), (oc - 1u) & 1u, limit, abort_flag, 6))
             return false;
           tc_fence_after();
           issue_pv(i, v_slot, accumulate);
@@ -1112,7 +1137,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         };
         Item it;
         for (int n = 0; ok && take_item(n, it, ok); ++n) {
-          const int nq = it.u.two ? 2 : 1;
+          const bool mine = i == 0 || it.u.two;
           ok = warp_wait(bar_q, n & 1, limit, abort_flag, 2);
           if (!ok) break;
           int j = 0;  // key tiles visited so far in this item
@@ -1126,45 +1151,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = v_slot >= 0;
             if (!ok) break;
             tc_fence_after();
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              if (i >= nq || !ok) break;
+            if (mine) {
               if (j > 0) {
-                ok = warp_wait(bar_p(i), (si[i] - 1u) & 1u, limit, abort_flag, 4);
+                ok = warp_wait(bar_p(i), (si - 1u) & 1u, limit, abort_flag, 4);
                 if (!ok) break;
                 tc_fence_after();
               }
               issue_s(i, k_slot);
               mma_commit_elect(bar_s(i));
-              ++si[i];
+              ++si;
               if (j > 0) {
-                ok = pv(i, v_slot, j - 1 > 0);
+                ok = pv(v_slot, j - 1 > 0);
                 if (!ok) break;
                 mma_commit_elect(bar_pvdone(i));
               }
             }
-            if (!ok) break;
-            mma_commit_elect(bar_kv_empty(k_slot));
-            if (j > 0) mma_commit_elect(bar_kv_empty(v_slot));
+            release(bar_kv_empty(k_slot), mine);
+            if (j > 0) release(bar_kv_empty(v_slot), mine);
             ld += 2u;
             ++j;
           }
           if (!ok) break;
-          mma_commit_elect(bar_qfree);  // every S MMA of this item has been issued
+          release(bar_qfree, mine);  // every S MMA of this item has been issued
           const int v_slot = ring_wait(ld - 1u, 5);
           ok = v_slot >= 0;
           if (!ok) break;
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            if (i >= nq || !ok) break;
-            ok = warp_wait(bar_p(i), (si[i] - 1u) & 1u, limit, abort_flag, 4);
+          if (mine) {
+            ok = warp_wait(bar_p(i), (si - 1u) & 1u, limit, abort_flag, 4);
             if (!ok) break;
-            ok = pv(i, v_slot, j - 1 > 0);
+            ok = pv(v_slot, j - 1 > 0);
             if (!ok) break;
             mma_commit_elect(bar_o(i));
-            ++oc[i];
+            ++oc;
           }
-          if (ok) mma_commit_elect(bar_kv_empty(v_slot));
+          release(bar_kv_empty(v_slot), mine);
         }
       } else {
       int slot = 0;
@@ -1505,7 +1525,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int s = 0; s < C::NSLOT; ++s)
         if (ld_issued & (1u << s)) wait_drain(bar_kv_full(s), (ld_parity >> s) & 1u, limit);
     }
-    if (warp == MMA_WARP) {
+    if (warp == MMA_WARP || (DUAL && warp == MMA_WARP2)) {
       // The MMAs were issued by the elected lane: commit from it too.
       mma_commit_elect(smem_u32(&ctl->drain));
       if (lane == 0) wait_drain(smem_u32(&ctl->drain), 0, limit);
