@@ -80,7 +80,11 @@ struct Cfg {
   static constexpr uint32_t TAIL_OFF = SUM_OFF + 3 * 4 * MAX_SEQ_TILES;  // and tail prefix sums
   static constexpr uint32_t ITEMS_OFF = TAIL_OFF + 4 * (MAX_TAIL_UNITS + 4);  // and tail items
   static constexpr uint32_t ORDER_OFF = ITEMS_OFF + 48 * 32;  // and the unit order tables
-  static constexpr uint32_t SMEM_BYTES_BC = ORDER_OFF + 4 * (3 * MAX_Q_PAIRS + 2) + 1024;
+  // and, per work-item slot, bit masks over the key tiles: visited by the
+  // item's query pair, and seen whole by query tile 0 / by query tile 1
+  static constexpr uint32_t MASK_OFF = ORDER_OFF + 4 * (3 * MAX_Q_PAIRS + 2);
+  static constexpr int MASK_WORDS = MAX_SEQ_TILES / 32;
+  static constexpr uint32_t SMEM_BYTES_BC = MASK_OFF + 2 * 3 * 4 * MASK_WORDS + 1024;
   // Share of the exponentials computed by the FMA-pipe polynomial instead of
   // the MUFU unit: POLY_NUM of every POLY_DEN packed pairs.  On GB300 the
   // MUFU unit does about 30 exp2 per clock per SM and the polynomial about 13:
@@ -976,13 +980,46 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
   };
   // Work item n, decoded once by the loader and read by the other roles
   // (whole warps).  The loader writes item n into slot n & 1 once every
-  // reader has taken item n - 2 (item_empty), then arrives on item_full; a
-  // slot with t_begin < 0 means no item is left.  take_item returns false at
-  // the end or, with ok false, when a wait gave up.
+  // reader is done with item n - 2 (item_empty), then arrives on item_full;
+  // a slot with t_begin < 0 means no item is left.  A reader keeps the slot
+  // of its current item (masked forms: its tile masks, below) until it takes
+  // the next one.  take_item returns false at the end or, with ok false, when
+  // a wait gave up.
+  //
+  // Masked forms: with each item the loader leaves three bit masks over the
+  // key tiles [t_begin, t_end) in its slot (MASK_OFF): visited by the item's
+  // query pair, and seen whole by query tile 0, by query tile 1.  The roles
+  // test a bit per key tile instead of the tile tables.
+  uint32_t* const tile_masks = reinterpret_cast<uint32_t*>(base + C::MASK_OFF);
+  auto slot_masks = [&](int n) -> const uint32_t* {
+    return tile_masks + (n & 1) * 3 * C::MASK_WORDS;
+  };
+  auto tile_bit = [](const uint32_t* m, int t) -> bool { return (m[t >> 5] >> (t & 31)) & 1u; };
   auto publish_item = [&](int n, const Item* src) -> bool {
     const int sl = n & 1;
     if (n >= 2 && !warp_wait(bar_iempty(sl), ((n >> 1) - 1) & 1, limit, abort_flag, 17))
       return false;
+    if constexpr (BC) {
+      if (src) {
+        uint32_t* mk = tile_masks + sl * 3 * C::MASK_WORDS;
+        const Unit& u = src->u;
+        const int qt0 = u.q0 / BM;
+        for (int w = src->t_begin >> 5; w <= (src->t_end - 1) >> 5; ++w) {
+          const int t = w * 32 + lane;
+          const bool vis = t >= src->t_begin && t < src->t_end && bc_unit_visits(tt, p, u, t);
+          const bool f0 = vis && bc_tile_full(tt, p, qt0, u.q0, t);
+          const bool f1 = vis && u.two && bc_tile_full(tt, p, qt0 + 1, u.q0 + BM, t);
+          const uint32_t bv = __ballot_sync(0xffffffffu, vis);
+          const uint32_t b0 = __ballot_sync(0xffffffffu, f0);
+          const uint32_t b1 = __ballot_sync(0xffffffffu, f1);
+          if (lane == 0) {
+            mk[w] = bv;
+            mk[C::MASK_WORDS + w] = b0;
+            mk[2 * C::MASK_WORDS + w] = b1;
+          }
+        }
+      }
+    }
     if (lane == 0) {
       if (src) item_ring[sl] = *src; else item_ring[sl].t_begin = -1;
       mbar_arrive(bar_ifull(sl));
@@ -992,11 +1029,11 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
   };
   auto take_item = [&](int n, Item& out, bool& ok) -> bool {
     const int sl = n & 1;
+    if (n >= 1 && lane == 0) mbar_arrive(bar_iempty(sl ^ 1));  // done with item n - 1
     ok = warp_wait(bar_ifull(sl), (n >> 1) & 1, limit, abort_flag, 16);
     if (!ok) return false;
     out = item_ring[sl];
     __syncwarp();
-    if (lane == 0) mbar_arrive(bar_iempty(sl));
     return out.t_begin >= 0;
   };
   // Loader bookkeeping for draining copies in flight after an abort.
@@ -1041,7 +1078,7 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
         q_last = n;
 #pragma unroll 1
         for (int t = it.t_begin; t < it.t_end && ok; ++t) {
-          if (BC && !bc_unit_visits(tt, p, u, t)) continue;
+          if (BC && !tile_bit(slot_masks(n), t)) continue;
           const int seg = (t < T0) ? 0 : 1;
           const int tok0 = (t - (seg ? T0 : 0)) * BN;
           for (int kind = 0; kind < 2; ++kind) {
@@ -1143,7 +1180,7 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
           int j = 0;  // key tiles visited so far in this item
 #pragma unroll 1
           for (int t = it.t_begin; t < it.t_end && ok; ++t) {
-            if (BC && !bc_unit_visits(tt, p, it.u, t)) continue;
+            if (BC && !tile_bit(slot_masks(n), t)) continue;
             const int k_slot = ring_wait(ld, 3);
             ok = k_slot >= 0;
             if (!ok) break;
@@ -1212,7 +1249,7 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
         int j = 0;  // key tiles visited so far in this item
 #pragma unroll 1
         for (int t = it.t_begin; t < it.t_end && ok; ++t) {
-          if (BC && !bc_unit_visits(tt, p, it.u, t)) continue;
+          if (BC && !tile_bit(slot_masks(n), t)) continue;
           const int k_slot = slot;
           ok = warp_wait(bar_kv_full(k_slot), phase, limit, abort_flag, 3);
           if (!ok) break;
@@ -1354,8 +1391,9 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
 #pragma unroll 1
       for (int t = it.t_begin; t < it.t_end; ++t) {
         if constexpr (BC) {
-          if (!bc_unit_visits(tt, p, u, t)) continue;
-          const bool full = bc_tile_full(tt, p, u.q0 / BM + i, u.q0 + i * BM, t);
+          const uint32_t* mk = slot_masks(n);
+          if (!tile_bit(mk, t)) continue;
+          const bool full = tile_bit(mk + (1 + i) * C::MASK_WORDS, t);
           mask.c0 = key_tile_pos(p, t);
           mask.ids = !full;
           mask.valid = p.key_valid != nullptr;
