@@ -519,24 +519,31 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
 
 
+# The audit timing of the kernel pages: at least 10 warm-up calls, then the
+# median of at least 50 per-call CUDA-event samples.
+CONFIG_WARMUP = 10
+CONFIG_SAMPLES = 50
+
+
 def per_config(torch, ncp, flush, stream, peak, args):
     """Device TFLOP/s of every synthetic workload (context for the line): the
-    median, mean and min of per-launch CUDA-event times with the L2 flushed
-    before each launch, and graph_us, the per-launch time of graph_iters
-    back-to-back launches replayed from one CUDA graph (warm L2)."""
+    median, mean and min of CONFIG_SAMPLES per-launch CUDA-event times after
+    CONFIG_WARMUP warm-up launches, with the L2 flushed before each launch,
+    and graph_us, the per-launch time of graph_iters back-to-back launches
+    replayed from one CUDA graph (warm L2)."""
     res = {}
     for cid, w in workloads.WORKLOADS.items():
         dev_in = [t.cuda() for t in workloads.make_inputs(w)]
         out = torch.empty_like(dev_in[0])
         call = make_call(ncp, w, dev_in, out)
-        steps = max(3, min(args.steps, 20))
-        times, _ = time_device(torch, call, flush, steps, 3, stream)
+        times, _ = time_device(torch, call, flush, CONFIG_SAMPLES, CONFIG_WARMUP, stream)
         us = statistics.median(times) * 1e3
         tf = w.flops / (us / 1e6) / 1e12
         iters = max(1, min(50, int(2000.0 / us)))
         g_us = time_graph(torch, call, stream, iters) * 1e3
         res[w.name] = {"median_us": round(us, 2), "mean_us": round(statistics.mean(times) * 1e3, 2),
-                       "min_us": round(min(times) * 1e3, 2),
+                       "min_us": round(min(times) * 1e3, 2), "samples": len(times),
+                       "warmup": CONFIG_WARMUP,
                        "tflops": round(tf, 1), "frac_of_peak": round(tf / peak, 4),
                        "graph_us": round(g_us, 2), "graph_iters": iters,
                        "tensor_pipe_active_pct": recorded_profile(w.name).get(
