@@ -117,7 +117,7 @@ struct SharedCtl {
   uint64_t drain;
   uint64_t tail_ready;     // masked forms: this CTA's tail items are in shared memory
   uint64_t item_full[2];   // the loader has written work item slot s (item n: slot n & 1)
-  uint64_t item_empty[2];  // the 8 softmax warps and the MMA warp have read slot s
+  uint64_t item_empty[2];  // every warp but the loader is done with slot s's item
   int last[2];             // this piece is the last of its unit: merge and store
   int n_tail_items;        // masked forms: tail items of this CTA kept in shared memory
   uint32_t tmem_base;
