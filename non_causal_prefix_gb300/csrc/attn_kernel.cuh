@@ -62,9 +62,9 @@ struct Cfg {
   // S_1, O_0, O_1 take 128 each, and P_i (bf16, two per column) is written
   // over the first 64 columns of S_i, so S_i(j + 1) follows the P V that
   // reads P_i(j).  D = 64: O_i takes 64 columns, which leaves 64 for each P_i
-  // (P_OWN), and S_i(j + 1) is issued as soon as P_i(j) is written, ahead of
-  // its P V: a query tile's key step is then softmax + S, not softmax + P V
-  // + S.
+  // (P_OWN), and S_i(j + 1) is issued as soon as the softmax warps have read
+  // S_i(j) into registers, so that it runs during their softmax: a query
+  // tile's key step is then about its softmax, not softmax + P V + S.
   static constexpr bool P_OWN = (D == 64) && NCP_P_OWN;
   __host__ __device__ static constexpr uint32_t s_col(int i) { return 128u * i; }
   __host__ __device__ static constexpr uint32_t p_col(int i) { return P_OWN ? 256u + 64u * i : 128u * i; }
@@ -115,6 +115,7 @@ struct SharedCtl {
   uint64_t o_full[2];
   uint64_t o_free[2];
   uint64_t pv_done[2];     // D = 64: a P V of query tile i, not an item's last, is complete
+  uint64_t s_free[2];      // D = 64: the 4 softmax warps of query tile i have read S_i
   uint64_t part_done[2];   // the 4 warps of a query tile wrote their partial rows
   uint64_t merge_ready[2]; // the piece's arrival count is known (SharedCtl::last)
   uint64_t drain;
@@ -598,17 +599,19 @@ __device__ __forceinline__ void build_row_mask(const Params& p, const RowMask& m
 // p_addr (64 columns); O is rescaled in TMEM when m moved.  before_store()
 // runs before P and O are written and returns false if they must not be (a
 // wait gave up); the tile then stops there and returns false.
-template <int D, bool BC, class BeforeStore>
+template <int D, bool BC, class AfterRead, class BeforeStore>
 __device__ __forceinline__ bool softmax_tile(uint32_t s_addr, uint32_t p_addr, uint32_t o_addr,
                                              int valid, float sl2, bool may_rescale,
                                              const uint32_t (&vis)[4], bool masked, float& m,
-                                             float& l, BeforeStore before_store) {
+                                             float& l, AfterRead after_read,
+                                             BeforeStore before_store) {
   float s[BN];
   {
     uint32_t r[BN];
 #pragma unroll
     for (int c = 0; c < BN; c += 32) tmem_ld32(s_addr + c, r + c);
     tmem_wait_ld();
+    after_read();
 #pragma unroll
     for (int c = 0; c < BN; ++c) s[c] = __uint_as_float(r[c]);
   }
@@ -848,6 +851,7 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
   auto bar_iempty = [&](int s) { return smem_u32(&ctl->item_empty[s]); };
   Item* const item_ring = reinterpret_cast<Item*>(ctl->item_ring);
   auto bar_pvdone = [&](int i) { return smem_u32(&ctl->pv_done[i]); };
+  auto bar_sfree = [&](int i) { return smem_u32(&ctl->s_free[i]); };
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
@@ -862,6 +866,7 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
       mbar_init(bar_o(i), 1);
       mbar_init(bar_ofree(i), 4);  // one arrival per softmax warp
       mbar_init(bar_pvdone(i), 1);
+      mbar_init(bar_sfree(i), 4);  // one arrival per softmax warp
       mbar_init(smem_u32(&ctl->part_done[i]), 4);
       mbar_init(smem_u32(&ctl->merge_ready[i]), 1);
     }
@@ -1136,10 +1141,11 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
 
       if constexpr (C::P_OWN) {
         // D = 64, P in columns of its own; one MMA warp per query tile i.
-        // Per visited key tile j: once P_i(j - 1) is written, S_i(j) goes
-        // first (the softmax warps have read S_i), then P_i V(j - 1), which
-        // commits pv_done (the softmax warps wait for it before writing P_i
-        // again or rescaling O_i); an item's last P V commits o_full.  The K
+        // Per visited key tile j: once the softmax warps have read S_i(j - 1)
+        // (s_free), S_i(j) goes, and runs while they work on S_i(j - 1); then,
+        // once P_i(j - 1) is written, P_i V(j - 1), which commits pv_done (the
+        // softmax warps wait for it before writing P_i again or rescaling O_i);
+        // an item's last P V commits o_full.  The K
         // and V of a tile are ring loads 2 j and 2 j + 1 of the item, in load
         // order; ld counts the loads consumed.  A ring slot and the Q buffers
         // are free once both warps have released them (kv_empty and q_free
@@ -1187,27 +1193,36 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
             const int k_slot = ring_wait(ld, 3);
             ok = k_slot >= 0;
             if (!ok) break;
-            const int v_slot = j > 0 ? ring_wait(ld - 1u, 5) : 0;
-            ok = v_slot >= 0;
-            if (!ok) break;
             tc_fence_after();
             if (mine) {
+              // S_i(j) overwrites S_i(j - 1): wait until the softmax warps
+              // have read it (S number si - 1).  An item's first S follows
+              // the previous item's last P, which they wrote after reading.
               if (j > 0) {
-                ok = warp_wait(bar_p(i), (si - 1u) & 1u, limit, abort_flag, 4);
+                ok = warp_wait(bar_sfree(i), (si - 1u) & 1u, limit, abort_flag, 18);
                 if (!ok) break;
                 tc_fence_after();
               }
               issue_s(i, k_slot);
               mma_commit_elect(bar_s(i));
               ++si;
-              if (j > 0) {
+            }
+            release(bar_kv_empty(k_slot), mine);
+            if (j > 0) {
+              const int v_slot = ring_wait(ld - 1u, 5);
+              ok = v_slot >= 0;
+              if (!ok) break;
+              if (mine) {
+                // P_i(j - 1) is P number si - 2 (S_i(j) is counted already).
+                ok = warp_wait(bar_p(i), (si - 2u) & 1u, limit, abort_flag, 4);
+                if (!ok) break;
+                tc_fence_after();
                 ok = pv(v_slot, j - 1 > 0);
                 if (!ok) break;
                 mma_commit_elect(bar_pvdone(i));
               }
+              release(bar_kv_empty(v_slot), mine);
             }
-            release(bar_kv_empty(k_slot), mine);
-            if (j > 0) release(bar_kv_empty(v_slot), mine);
             ld += 2u;
             ++j;
           }
@@ -1426,8 +1441,17 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
           }
           return true;
         };
+        // D = 64: S_i may be overwritten by the next S once these warps
+        // have read it.
+        auto after_read = [&]() {
+          if constexpr (C::P_OWN) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_sfree(i));
+          }
+        };
         ok = softmax_tile<D, BC>(s_addr, p_addr, o_addr, valid, sl2, !first, vis, masked, m, l,
-                                 before_store);
+                                 after_read, before_store);
         ++j;
         if (!ok) break;
         tmem_wait_st();
