@@ -76,6 +76,12 @@ struct Cfg {
   // for the register spills of the 11-warp kernel.
   static constexpr int NSLOT = (D == 128) ? 4 : 6;
   static constexpr uint32_t RING_OFF = 0;
+  // D = 64: the ring holds K/V pairs (a key tile's K and V in one entry, one
+  // full barrier expecting both, one release): NSLOT / 2 entries.
+  static constexpr bool KV_PAIRS = P_OWN;
+  static constexpr int NRING = KV_PAIRS ? NSLOT / 2 : NSLOT;
+  static constexpr uint32_t ENTRY_BYTES = KV_PAIRS ? 2 * TILE_BYTES : TILE_BYTES;
+  static_assert(!KV_PAIRS || NSLOT % 2 == 0, "K/V pairs take two slots each");
   static constexpr uint32_t Q_OFF = RING_OFF + NSLOT * TILE_BYTES;
   static constexpr uint32_t BAR_OFF = Q_OFF + 2 * TILE_BYTES;
   static constexpr uint32_t SMEM_BYTES = BAR_OFF + 512 + 1024;  // barriers + 1 KiB alignment slack
@@ -856,7 +862,7 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
     mbar_init(bar_qfree, DUAL ? 2 : 1);  // one release per MMA warp
-    for (int s = 0; s < C::NSLOT; ++s) {
+    for (int s = 0; s < C::NRING; ++s) {
       mbar_init(bar_kv_full(s), 1);
       mbar_init(bar_kv_empty(s), DUAL ? 2 : 1);
     }
@@ -1089,6 +1095,27 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
           if (BC && !tile_bit(slot_masks(n), t)) continue;
           const int seg = (t < T0) ? 0 : 1;
           const int tok0 = (t - (seg ? T0 : 0)) * BN;
+          if constexpr (C::KV_PAIRS) {
+            ok = warp_wait(bar_kv_empty(slot), phase ^ 1u, limit, abort_flag, 1);
+            if (!ok) break;
+            mbar_expect_tx_elect(bar_kv_full(slot), 2 * C::TILE_BYTES);
+            for (int kind = 0; kind < 2; ++kind) {
+              const bool skip = (p.fault_mode == 1) && kind == 1 && t == 1 && n == 0 && blockIdx.x == 0;
+              if (skip) continue;
+              const CUtensorMap* map = kind == 0 ? &p.tm_k[seg] : &p.tm_v[seg];
+              for (int c = 0; c < C::CHUNKS; ++c)
+                tma_load_4d_elect(ring + slot * C::ENTRY_BYTES + kind * C::TILE_BYTES +
+                                      c * C::CHUNK_BYTES,
+                                  map, c * 64, u.h, tok0, u.b, bar_kv_full(slot));
+            }
+            ld_issued |= 1u << slot;
+            ld_parity = (ld_parity & ~(1u << slot)) | (phase << slot);
+            if (++slot == C::NRING) {
+              slot = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           for (int kind = 0; kind < 2; ++kind) {
             ok = warp_wait(bar_kv_empty(slot), phase ^ 1u, limit, abort_flag, 1);
             if (!ok) break;
@@ -1119,9 +1146,8 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
       constexpr uint32_t IDESC_S = make_idesc(BM, BN, false);
       constexpr uint32_t IDESC_PV = make_idesc(BM, D, true);
       // S_i = Q_i K^T over D in K-steps of 16 (32 bytes inside a 128-byte row).
-      auto issue_s = [&](int i, int k_slot) {
+      auto issue_s = [&](int i, uint32_t kb) {
         const uint32_t qa = qs + i * C::TILE_BYTES;
-        const uint32_t kb = ring + k_slot * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
@@ -1130,8 +1156,7 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
         }
       };
       // O_i += P_i V over the BN keys in K-steps of 16 rows of V (MN-major B).
-      auto issue_pv = [&](int i, int v_slot, bool accumulate) {
-        const uint32_t vb = ring + v_slot * C::TILE_BYTES;
+      auto issue_pv = [&](int i, uint32_t vb, bool accumulate) {
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_ts_elect(tmem + C::o_col(i), tmem + C::p_col(i) + kk * 8,
@@ -1145,22 +1170,22 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
         // (s_free), S_i(j) goes, and runs while they work on S_i(j - 1); then,
         // once P_i(j - 1) is written, P_i V(j - 1), which commits pv_done (the
         // softmax warps wait for it before writing P_i again or rescaling O_i);
-        // an item's last P V commits o_full.  The K
-        // and V of a tile are ring loads 2 j and 2 j + 1 of the item, in load
-        // order; ld counts the loads consumed.  A ring slot and the Q buffers
-        // are free once both warps have released them (kv_empty and q_free
-        // take two arrivals): by a commit after their MMAs, or, for an item
-        // without this warp's query tile, by a plain arrival made after the
-        // slot's or Q's full phase, so that it never counts toward the phase
-        // before.
+        // an item's last P V commits o_full.  The K and V of a key tile share
+        // one ring entry (KV_PAIRS), loaded in key-tile order; ld counts the
+        // entries consumed.  Entry j - 1 is released after P_i V(j - 1), its
+        // last reader.  A ring entry and the Q buffers are free once both
+        // warps have released them (kv_empty and q_free take two arrivals): by
+        // a commit after their MMAs, or, for an item without this warp's query
+        // tile, by a plain arrival made after the entry's or Q's full phase, so
+        // that it never counts toward the phase before.
         const int i = warp - MMA_WARP;  // this warp's query tile
         uint32_t si = 0;  // S issued (phases of s_full / p_full)
         uint32_t oc = 0;  // items finished (phases of o_full / o_free)
-        uint32_t ld = 0;
+        uint32_t ld = 0;  // ring entries (key tiles, K and V together) consumed
         bool ok = true;
         auto ring_wait = [&](uint32_t x, int site) -> int {
-          const int sl = static_cast<int>(x % C::NSLOT);
-          if (!warp_wait(bar_kv_full(sl), (x / C::NSLOT) & 1u, limit, abort_flag, site)) return -1;
+          const int sl = static_cast<int>(x % C::NRING);
+          if (!warp_wait(bar_kv_full(sl), (x / C::NRING) & 1u, limit, abort_flag, site)) return -1;
           return sl;
         };
         auto release = [&](uint32_t bar, bool mine) {
@@ -1173,12 +1198,12 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
         };
         // P_i V(j - 1): P_i(j - 1) was waited for; the first of an item waits
         // for the epilogue that read O_i.
-        auto pv = [&](int v_slot, bool accumulate) -> bool {
+        auto pv = [&](uint32_t vb, bool accumulate) -> bool {
           if (!accumulate && oc > 0 &&
               !warp_wait(bar_ofree(i), (oc - 1u) & 1u, limit, abort_flag, 6))
             return false;
           tc_fence_after();
-          issue_pv(i, v_slot, accumulate);
+          issue_pv(i, vb, accumulate);
           return true;
         };
         Item it;
@@ -1186,12 +1211,13 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
           const bool mine = i == 0 || it.u.two;
           ok = warp_wait(bar_q, n & 1, limit, abort_flag, 2);
           if (!ok) break;
-          int j = 0;  // key tiles visited so far in this item
+          int j = 0;      // key tiles visited so far in this item
+          int prev = 0;   // ring entry of key tile j - 1
 #pragma unroll 1
           for (int t = it.t_begin; t < it.t_end && ok; ++t) {
             if (BC && !tile_bit(slot_masks(n), t)) continue;
-            const int k_slot = ring_wait(ld, 3);
-            ok = k_slot >= 0;
+            const int e = ring_wait(ld, 3);
+            ok = e >= 0;
             if (!ok) break;
             tc_fence_after();
             if (mine) {
@@ -1203,43 +1229,36 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
                 if (!ok) break;
                 tc_fence_after();
               }
-              issue_s(i, k_slot);
+              issue_s(i, ring + e * C::ENTRY_BYTES);
               mma_commit_elect(bar_s(i));
               ++si;
-            }
-            release(bar_kv_empty(k_slot), mine);
-            if (j > 0) {
-              const int v_slot = ring_wait(ld - 1u, 5);
-              ok = v_slot >= 0;
-              if (!ok) break;
-              if (mine) {
+              if (j > 0) {
                 // P_i(j - 1) is P number si - 2 (S_i(j) is counted already).
                 ok = warp_wait(bar_p(i), (si - 2u) & 1u, limit, abort_flag, 4);
                 if (!ok) break;
                 tc_fence_after();
-                ok = pv(v_slot, j - 1 > 0);
+                ok = pv(ring + prev * C::ENTRY_BYTES + C::TILE_BYTES, j - 1 > 0);
                 if (!ok) break;
                 mma_commit_elect(bar_pvdone(i));
               }
-              release(bar_kv_empty(v_slot), mine);
             }
-            ld += 2u;
+            // Key tile j - 1's entry: its S and its P V have been issued.
+            if (j > 0) release(bar_kv_empty(prev), mine);
+            prev = e;
+            ++ld;
             ++j;
           }
           if (!ok) break;
           release(bar_qfree, mine);  // every S MMA of this item has been issued
-          const int v_slot = ring_wait(ld - 1u, 5);
-          ok = v_slot >= 0;
-          if (!ok) break;
           if (mine) {
             ok = warp_wait(bar_p(i), (si - 1u) & 1u, limit, abort_flag, 4);
             if (!ok) break;
-            ok = pv(v_slot, j - 1 > 0);
+            ok = pv(ring + prev * C::ENTRY_BYTES + C::TILE_BYTES, j - 1 > 0);
             if (!ok) break;
             mma_commit_elect(bar_o(i));
             ++oc;
           }
-          release(bar_kv_empty(v_slot), mine);
+          release(bar_kv_empty(prev), mine);
         }
       } else {
       int slot = 0;
@@ -1255,7 +1274,7 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
             !warp_wait(bar_ofree(i), (oc[i] - 1u) & 1u, limit, abort_flag, 6))
           return false;
         tc_fence_after();
-        issue_pv(i, v_slot, accumulate);
+        issue_pv(i, ring + v_slot * C::TILE_BYTES, accumulate);
         return true;
       };
       Item it;
@@ -1282,7 +1301,7 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
               ok = pv(i, v_prev, j - 1 > 0);
               if (!ok) break;
             }
-            issue_s(i, k_slot);
+            issue_s(i, ring + k_slot * C::TILE_BYTES);
             mma_commit_elect(bar_s(i));
             ++sc[i];
           }
@@ -1587,7 +1606,7 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
     // TMA copy and every MMA still in flight land (bounded waits again).
     if (warp == PRODUCER_WARP && lane == 0) {
       if (q_last >= 0) wait_drain(bar_q, q_last & 1, limit);
-      for (int s = 0; s < C::NSLOT; ++s)
+      for (int s = 0; s < C::NRING; ++s)
         if (ld_issued & (1u << s)) wait_drain(bar_kv_full(s), (ld_parity >> s) & 1u, limit);
     }
     if (warp == MMA_WARP || (DUAL && warp == MMA_WARP2)) {

@@ -174,11 +174,14 @@ def test_side_stream(cuda_lib, oracle_mod):
     assert_parity(f64(out), oracle_mod.dense_attention(*bits(ins)), "side stream")
 
 
-def test_bounded_wait_reports_timeout(cuda_lib, oracle_mod):
+@pytest.mark.parametrize("D", [128, 64])
+def test_bounded_wait_reports_timeout(cuda_lib, oracle_mod, D):
     """A wait that can never complete (the loader skips one value tile on
     purpose) ends with ATTN_ERR_TIMEOUT instead of a hang, and the context
-    stays usable for the next call."""
-    w = workloads.custom("dense", 1, 256, 256, 1, 128)
+    stays usable for the next call.  D = 128 loads K and V into ring slots of
+    their own; D = 64 loads them into one entry, whose full barrier then never
+    completes."""
+    w = workloads.custom("dense", 1, 256, 256, 1, D)
     ins = workloads.make_inputs(w, seed_base=9900)
     q, k, v = to_dev(ins)
     assert cuda_lib.device_status()[0] == cuda_lib.ATTN_OK
