@@ -1114,24 +1114,24 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
               slot = 0;
               phase ^= 1u;
             }
-            continue;
-          }
-          for (int kind = 0; kind < 2; ++kind) {
-            ok = warp_wait(bar_kv_empty(slot), phase ^ 1u, limit, abort_flag, 1);
-            if (!ok) break;
-            const bool skip = (p.fault_mode == 1) && kind == 1 && t == 1 && n == 0 && blockIdx.x == 0;
-            if (!skip) {
-              const CUtensorMap* map = kind == 0 ? &p.tm_k[seg] : &p.tm_v[seg];
-              mbar_expect_tx_elect(bar_kv_full(slot), C::TILE_BYTES);
-              for (int c = 0; c < C::CHUNKS; ++c)
-                tma_load_4d_elect(ring + slot * C::TILE_BYTES + c * C::CHUNK_BYTES, map, c * 64,
-                                  u.h, tok0, u.b, bar_kv_full(slot));
-              ld_issued |= 1u << slot;
-              ld_parity = (ld_parity & ~(1u << slot)) | (phase << slot);
-            }
-            if (++slot == C::NSLOT) {
-              slot = 0;
-              phase ^= 1u;
+          } else {
+            for (int kind = 0; kind < 2; ++kind) {
+              ok = warp_wait(bar_kv_empty(slot), phase ^ 1u, limit, abort_flag, 1);
+              if (!ok) break;
+              const bool skip = (p.fault_mode == 1) && kind == 1 && t == 1 && n == 0 && blockIdx.x == 0;
+              if (!skip) {
+                const CUtensorMap* map = kind == 0 ? &p.tm_k[seg] : &p.tm_v[seg];
+                mbar_expect_tx_elect(bar_kv_full(slot), C::TILE_BYTES);
+                for (int c = 0; c < C::CHUNKS; ++c)
+                  tma_load_4d_elect(ring + slot * C::TILE_BYTES + c * C::CHUNK_BYTES, map, c * 64,
+                                    u.h, tok0, u.b, bar_kv_full(slot));
+                ld_issued |= 1u << slot;
+                ld_parity = (ld_parity & ~(1u << slot)) | (phase << slot);
+              }
+              if (++slot == C::NSLOT) {
+                slot = 0;
+                phase ^= 1u;
+              }
             }
           }
         }
