@@ -76,12 +76,16 @@ struct Cfg {
   // for the register spills of the 11-warp kernel.
   static constexpr int NSLOT = (D == 128) ? 4 : 6;
   static constexpr uint32_t RING_OFF = 0;
-  // D = 64: the ring holds K/V pairs (a key tile's K and V in one entry, one
-  // full barrier expecting both, one release): NSLOT / 2 entries.
+  // The ring holds NSLOT / 2 entries of two tiles (K half, then V half), one
+  // full barrier expecting both loads and one release each.  D = 64
+  // (KV_PAIRS): a key tile's K and V.  D = 128: K of a key tile and V of the
+  // item's previous visited key tile (S_i(j) and P_i V(j - 1) are issued
+  // together), an item's first entry holding K alone and an entry after its
+  // last key tile holding the last V alone.
   static constexpr bool KV_PAIRS = P_OWN;
-  static constexpr int NRING = KV_PAIRS ? NSLOT / 2 : NSLOT;
-  static constexpr uint32_t ENTRY_BYTES = KV_PAIRS ? 2 * TILE_BYTES : TILE_BYTES;
-  static_assert(!KV_PAIRS || NSLOT % 2 == 0, "K/V pairs take two slots each");
+  static constexpr int NRING = NSLOT / 2;
+  static constexpr uint32_t ENTRY_BYTES = 2 * TILE_BYTES;
+  static_assert(NSLOT % 2 == 0, "ring entries take two slots each");
   static constexpr uint32_t Q_OFF = RING_OFF + NSLOT * TILE_BYTES;
   static constexpr uint32_t BAR_OFF = Q_OFF + 2 * TILE_BYTES;
   static constexpr uint32_t SMEM_BYTES = BAR_OFF + 512 + 1024;  // barriers + 1 KiB alignment slack
@@ -1090,6 +1094,7 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
             tma_load_4d_elect(qs + i * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tm_q, c * 64, u.h,
                               u.q0 + i * BM, u.b, bar_q);
         q_last = n;
+        int prev_t = -1;  // D = 128: the last key tile of this item loaded so far
 #pragma unroll 1
         for (int t = it.t_begin; t < it.t_end && ok; ++t) {
           if (BC && !tile_bit(slot_masks(n), t)) continue;
@@ -1115,24 +1120,48 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
               phase ^= 1u;
             }
           } else {
-            for (int kind = 0; kind < 2; ++kind) {
-              ok = warp_wait(bar_kv_empty(slot), phase ^ 1u, limit, abort_flag, 1);
-              if (!ok) break;
-              const bool skip = (p.fault_mode == 1) && kind == 1 && t == 1 && n == 0 && blockIdx.x == 0;
-              if (!skip) {
-                const CUtensorMap* map = kind == 0 ? &p.tm_k[seg] : &p.tm_v[seg];
-                mbar_expect_tx_elect(bar_kv_full(slot), C::TILE_BYTES);
+            ok = warp_wait(bar_kv_empty(slot), phase ^ 1u, limit, abort_flag, 1);
+            if (!ok) break;
+            mbar_expect_tx_elect(bar_kv_full(slot), (prev_t >= 0 ? 2 : 1) * C::TILE_BYTES);
+            if (prev_t >= 0) {
+              const bool skip = (p.fault_mode == 1) && prev_t == 1 && n == 0 && blockIdx.x == 0;
+              const int vseg = (prev_t < T0) ? 0 : 1;
+              const int vtok0 = (prev_t - (vseg ? T0 : 0)) * BN;
+              if (!skip)
                 for (int c = 0; c < C::CHUNKS; ++c)
-                  tma_load_4d_elect(ring + slot * C::TILE_BYTES + c * C::CHUNK_BYTES, map, c * 64,
-                                    u.h, tok0, u.b, bar_kv_full(slot));
-                ld_issued |= 1u << slot;
-                ld_parity = (ld_parity & ~(1u << slot)) | (phase << slot);
-              }
-              if (++slot == C::NSLOT) {
-                slot = 0;
-                phase ^= 1u;
-              }
+                  tma_load_4d_elect(
+                      ring + slot * C::ENTRY_BYTES + C::TILE_BYTES + c * C::CHUNK_BYTES,
+                      &p.tm_v[vseg], c * 64, u.h, vtok0, u.b, bar_kv_full(slot));
             }
+            for (int c = 0; c < C::CHUNKS; ++c)
+              tma_load_4d_elect(ring + slot * C::ENTRY_BYTES + c * C::CHUNK_BYTES, &p.tm_k[seg],
+                                c * 64, u.h, tok0, u.b, bar_kv_full(slot));
+            ld_issued |= 1u << slot;
+            ld_parity = (ld_parity & ~(1u << slot)) | (phase << slot);
+            if (++slot == C::NRING) {
+              slot = 0;
+              phase ^= 1u;
+            }
+            prev_t = t;
+          }
+        }
+        // D = 128: the item's last V, in an entry of its own.
+        if (!C::KV_PAIRS && ok && prev_t >= 0) {
+          ok = warp_wait(bar_kv_empty(slot), phase ^ 1u, limit, abort_flag, 1);
+          if (!ok) break;
+          mbar_expect_tx_elect(bar_kv_full(slot), C::TILE_BYTES);
+          const bool skip = (p.fault_mode == 1) && prev_t == 1 && n == 0 && blockIdx.x == 0;
+          const int vseg = (prev_t < T0) ? 0 : 1;
+          const int vtok0 = (prev_t - (vseg ? T0 : 0)) * BN;
+          if (!skip)
+            for (int c = 0; c < C::CHUNKS; ++c)
+              tma_load_4d_elect(ring + slot * C::ENTRY_BYTES + C::TILE_BYTES + c * C::CHUNK_BYTES,
+                                &p.tm_v[vseg], c * 64, u.h, vtok0, u.b, bar_kv_full(slot));
+          ld_issued |= 1u << slot;
+          ld_parity = (ld_parity & ~(1u << slot)) | (phase << slot);
+          if (++slot == C::NRING) {
+            slot = 0;
+            phase ^= 1u;
           }
         }
       }
@@ -1261,20 +1290,25 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
           release(bar_kv_empty(prev), mine);
         }
       } else {
-      int slot = 0;
-      uint32_t phase = 0;
+      uint32_t ld = 0;            // ring entries consumed
       uint32_t sc[2] = {0u, 0u};  // S commits per query tile (phases of s_full / p_full)
       uint32_t oc[2] = {0u, 0u};  // units finished per query tile (phases of o_full / o_free)
       bool ok = true;
+      auto ring_wait = [&](int site) -> int {
+        const int sl = static_cast<int>(ld % C::NRING);
+        if (!warp_wait(bar_kv_full(sl), (ld / C::NRING) & 1u, limit, abort_flag, site)) return -1;
+        ++ld;
+        return sl;
+      };
       // The first P V of a unit overwrites O_i: wait until the epilogue of the
       // previous unit has read it out of TMEM.
-      auto pv = [&](int i, int v_slot, bool accumulate) -> bool {
+      auto pv = [&](int i, uint32_t vb, bool accumulate) -> bool {
         if (!warp_wait(bar_p(i), (sc[i] - 1u) & 1u, limit, abort_flag, 4)) return false;
         if (!accumulate && oc[i] > 0 &&
             !warp_wait(bar_ofree(i), (oc[i] - 1u) & 1u, limit, abort_flag, 6))
           return false;
         tc_fence_after();
-        issue_pv(i, ring + v_slot * C::TILE_BYTES, accumulate);
+        issue_pv(i, vb, accumulate);
         return true;
       };
       Item it;
@@ -1282,50 +1316,48 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
         const int nq = it.u.two ? 2 : 1;
         ok = warp_wait(bar_q, n & 1, limit, abort_flag, 2);
         if (!ok) break;
-        int v_prev = -1;
         int j = 0;  // key tiles visited so far in this item
 #pragma unroll 1
         for (int t = it.t_begin; t < it.t_end && ok; ++t) {
           if (BC && !tile_bit(slot_masks(n), t)) continue;
-          const int k_slot = slot;
-          ok = warp_wait(bar_kv_full(k_slot), phase, limit, abort_flag, 3);
+          // Entry of key tile j: K_j, and V_{j-1} when j > 0.
+          const int e = ring_wait(3);
+          ok = e >= 0;
           if (!ok) break;
-          if (++slot == C::NSLOT) { slot = 0; phase ^= 1u; }
           tc_fence_after();
+          const uint32_t kb = ring + e * C::ENTRY_BYTES;
           // Unrolled over the two query tiles, so that sc[] / oc[] are
           // indexed by constants and stay in registers.
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
             if (i >= nq || !ok) break;
             if (j > 0) {
-              ok = pv(i, v_prev, j - 1 > 0);
+              ok = pv(i, kb + C::TILE_BYTES, j - 1 > 0);
               if (!ok) break;
             }
-            issue_s(i, ring + k_slot * C::TILE_BYTES);
+            issue_s(i, kb);
             mma_commit_elect(bar_s(i));
             ++sc[i];
           }
           if (!ok) break;
-          if (j > 0) mma_commit_elect(bar_kv_empty(v_prev));
-          mma_commit_elect(bar_kv_empty(k_slot));
-          const int v_slot = slot;
-          ok = warp_wait(bar_kv_full(v_slot), phase, limit, abort_flag, 5);
-          if (!ok) break;
-          if (++slot == C::NSLOT) { slot = 0; phase ^= 1u; }
-          v_prev = v_slot;
+          mma_commit_elect(bar_kv_empty(e));
           ++j;
         }
         if (!ok) break;
         mma_commit_elect(bar_qfree);  // every S MMA of this item has been issued
+        // The entry after the last key tile: the last V alone.
+        const int e = ring_wait(5);
+        ok = e >= 0;
+        if (!ok) break;
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           if (i >= nq || !ok) break;
-          ok = pv(i, v_prev, j - 1 > 0);
+          ok = pv(i, ring + e * C::ENTRY_BYTES + C::TILE_BYTES, j - 1 > 0);
           if (!ok) break;
           mma_commit_elect(bar_o(i));
           ++oc[i];
         }
-        if (ok) mma_commit_elect(bar_kv_empty(v_prev));
+        if (ok) mma_commit_elect(bar_kv_empty(e));
       }
       }
     }
