@@ -1175,22 +1175,36 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
       constexpr uint32_t IDESC_S = make_idesc(BM, BN, false);
       constexpr uint32_t IDESC_PV = make_idesc(BM, D, true);
       // S_i = Q_i K^T over D in K-steps of 16 (32 bytes inside a 128-byte row).
+      // The dense D = 128 kernel builds its descriptors once per group:
+      // shared-memory addresses stay below 2^18, so the start-address field
+      // (address / 16, 14 bits) of base + off is the base's plus off / 16,
+      // with no carry out of it.  Measured, this suits only that kernel (the
+      // D = 64 and masked ones were slower with it), so the others build each
+      // MMA's descriptors from its address.
+      constexpr bool BASE_DESC = (D == 128) && !BC;
       auto issue_s = [&](int i, uint32_t kb) {
         const uint32_t qa = qs + i * C::TILE_BYTES;
+        const uint64_t qd = sw128_desc(qa, 16, 1024);
+        const uint64_t kd = sw128_desc(kb, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-          mma_ss_elect(tmem + C::s_col(i), sw128_desc(qa + off, 16, 1024),
-                       sw128_desc(kb + off, 16, 1024), IDESC_S, kk > 0);
+          if constexpr (BASE_DESC)
+            mma_ss_elect(tmem + C::s_col(i), qd + (off >> 4), kd + (off >> 4), IDESC_S, kk > 0);
+          else
+            mma_ss_elect(tmem + C::s_col(i), sw128_desc(qa + off, 16, 1024),
+                         sw128_desc(kb + off, 16, 1024), IDESC_S, kk > 0);
         }
       };
       // O_i += P_i V over the BN keys in K-steps of 16 rows of V (MN-major B).
       auto issue_pv = [&](int i, uint32_t vb, bool accumulate) {
+        const uint64_t vd = sw128_desc(vb, C::CHUNK_BYTES, 1024);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_ts_elect(tmem + C::o_col(i), tmem + C::p_col(i) + kk * 8,
-                       sw128_desc(vb + kk * 16 * 128, C::CHUNK_BYTES, 1024), IDESC_PV,
-                       (accumulate || kk > 0) ? 1u : 0u);
+                       BASE_DESC ? vd + kk * (16 * 128 >> 4)
+                                 : sw128_desc(vb + kk * 16 * 128, C::CHUNK_BYTES, 1024),
+                       IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
       };
 
       if constexpr (C::P_OWN) {
