@@ -71,9 +71,10 @@ struct Cfg {
   __host__ __device__ static constexpr uint32_t o_col(int i) { return P_OWN ? 384u + 64u * i : 256u + 128u * i; }
   static constexpr uint32_t TILE_BYTES = BN * D * 2;     // one K or V tile; one Q tile (BM == BN)
   static constexpr uint32_t CHUNK_BYTES = BN * 128;      // 128 rows x 128 bytes
-  // K/V ring slots.  D = 64: 6 rather than 8 (measured as fast or faster on
-  // every D = 64 workload): the 32 KB less shared memory leaves a larger L1
-  // for the register spills of the 11-warp kernel.
+  // K/V ring, in tile-sized slots (paired into entries below).  D = 64: 6
+  // rather than 8 (measured as fast or faster on every D = 64 workload): the
+  // 32 KB less shared memory leaves a larger L1 for the register spills of
+  // the 11-warp kernel.
   static constexpr int NSLOT = (D == 128) ? 4 : 6;
   static constexpr uint32_t RING_OFF = 0;
   // The ring holds NSLOT / 2 entries of two tiles (K half, then V half), one
@@ -118,7 +119,7 @@ __host__ __device__ constexpr int num_threads() {
 struct SharedCtl {
   uint64_t q_full;
   uint64_t q_free;
-  uint64_t kv_full[MAX_SLOTS];
+  uint64_t kv_full[MAX_SLOTS];   // per K/V ring entry (Cfg::NRING of them are used)
   uint64_t kv_empty[MAX_SLOTS];
   uint64_t s_full[2];
   uint64_t p_full[2];
@@ -1055,7 +1056,7 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
     return out.t_begin >= 0;
   };
   // Loader bookkeeping for draining copies in flight after an abort.
-  uint32_t ld_issued = 0, ld_parity = 0;  // per ring slot: a load was issued / its phase
+  uint32_t ld_issued = 0, ld_parity = 0;  // per ring entry: a load was issued / its phase
   int q_last = -1;                        // last unit whose Q load was issued
 
   if (warp == PRODUCER_WARP) {
