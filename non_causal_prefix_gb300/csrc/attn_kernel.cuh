@@ -153,6 +153,9 @@ struct Sched {
   int n_whole;     // units walked whole
   int tail_units;  // units after them, cut into key ranges (0: none)
   int tail_ctas;   // CTAs sharing the tail (0: no tail)
+  // Dense forms with short key sequences (see make_sched): the loader
+  // prefetches each next work item's Q into L2.
+  int prefetch_q;
   // Dense forms: CTA c of the tail holds tail tiles [bounds[c], bounds[c + 1])
   // (tiles of the tail units in unit order), every range non-empty.
   int bounds[MAX_TAIL_CTAS + 1];
@@ -1080,6 +1083,19 @@ __global__ void __launch_bounds__(num_threads<D>(), 1)
         ok = await_tail(n, 12);
         if (!ok) break;
         const bool has = get_item<BC>(p, &mtail, T, n, it);
+        // Short units (prefetch_q): the next Q, read once from HBM, is
+        // prefetched into L2 while the current item's last key tiles run.
+        // Compiled into the dense D = 128 kernel only: present but unused, it
+        // slowed the D = 64 one by ~2 % through code generation.
+        if constexpr (!BC && D == 128) {
+          if (p.sc.prefetch_q && has && n > 0) {
+#pragma unroll
+            for (int c = 0; c < C::CHUNKS; ++c) {
+              tma_prefetch_4d_elect(&p.tm_q, c * 64, it.u.h, it.u.q0, it.u.b);
+              if (it.u.two) tma_prefetch_4d_elect(&p.tm_q, c * 64, it.u.h, it.u.q0 + BM, it.u.b);
+            }
+          }
+        }
         ok = publish_item(n, has ? &it : nullptr);
         if (!ok || !has) break;
         const Unit& u = it.u;

@@ -122,6 +122,18 @@ __device__ __forceinline__ unsigned long long ld_relaxed_gpu(const unsigned long
   return v;
 }
 
+// L2 prefetch of one tile of a tensor map (no shared memory, no barrier),
+// from the elected lane of a converged warp.
+__device__ __forceinline__ void tma_prefetch_4d_elect(const CUtensorMap* map, int c0, int c1,
+                                                      int c2, int c3) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];\n\t}" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
