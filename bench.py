@@ -314,7 +314,9 @@ def time_e2e(torch, ncp, w, host_in, steps, warmup, stream):
     to pinned host memory.  Two buffer sets and three streams (copies in,
     compute, copies out) let step i's compute overlap step i+1's input copy and
     step i-1's output copy, as a serving loop would; the CUDA events bracket
-    all ``steps`` steps, copies included."""
+    all ``steps`` steps, copies included.  Also returns the bandwidth of one
+    step's input copy and of its output copy, each timed alone before the
+    loop (GB/s): the link these copies go over sets the floor of a step."""
     nbuf = 2
     h2d_stream, d2h_stream = torch.cuda.Stream(), torch.cuda.Stream()
     dev_in = [[torch.empty_like(t, device="cuda") for t in host_in] for _ in range(nbuf)]
@@ -341,6 +343,19 @@ def time_e2e(torch, ncp, w, host_in, steps, warmup, stream):
             host_out[i].copy_(dev_out[i], non_blocking=True)
             out_done[i].record(d2h_stream)
 
+    # The copies alone, once warm: one step's inputs in, one output out.
+    copy_gbs = {}
+    for name, pairs in (("h2d", list(zip(dev_in[0], host_in))), ("d2h", [(host_out[0], dev_out[0])])):
+        for rep in range(2):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(h2d_stream):
+                a.record(h2d_stream)
+                for dst, src in pairs:
+                    dst.copy_(src, non_blocking=True)
+                b.record(h2d_stream)
+            torch.cuda.synchronize()
+        nbytes = sum(src.numel() * src.element_size() for _, src in pairs)
+        copy_gbs[name] = round(nbytes / (a.elapsed_time(b) / 1e3) / 1e9, 1)
     for s in range(warmup):
         one(s)
     torch.cuda.synchronize()
@@ -354,7 +369,7 @@ def time_e2e(torch, ncp, w, host_in, steps, warmup, stream):
     torch.cuda.synchronize()
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = host_out[0].numel() * host_out[0].element_size()
-    return start.elapsed_time(end) / steps, h2d, d2h
+    return start.elapsed_time(end) / steps, h2d, d2h, copy_gbs
 
 
 def cpu_oracle_sample(w, inputs_cpu, target_s: float):
@@ -444,7 +459,8 @@ def run_gpu(args):
 
     # End to end through the public API with host buffers.
     host_pinned = [t.pin_memory() for t in host_in]
-    e2e_ms, h2d, d2h = time_e2e(torch, ncp, w, host_pinned, max(4, args.steps), 3, stream)
+    e2e_ms, h2d, d2h, copy_gbs = time_e2e(torch, ncp, w, host_pinned, max(4, args.steps), 3,
+                                           stream)
     e2e_ms = max_over_ranks(e2e_ms, device="cuda")
     e2e_value = job_throughput(world, 1, w.flops, e2e_ms)
     clock_info = clocks.stop()
@@ -503,7 +519,8 @@ def run_gpu(args):
             **ncu_fields(w.name, hbm_peak),
         },
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+                "copy_gbs_alone": copy_gbs},
         "gpu_launches": args.steps,
         "clocks": clock_info,
     }
